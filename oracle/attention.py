@@ -1,0 +1,160 @@
+"""Plain fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` call it.  It shares no code, header, table or helper with the CUDA
+kernels; it receives the same rounded 16-bit inputs (as float64) and computes
+the textbook definition, materialising the full score matrix S and the
+probability matrix P of every head it evaluates.
+
+What it follows
+---------------
+* Forward, ``O = softmax(Q K^T * scale + mask) V``: the attention formula of the
+  page "FlashAttention — فلاش أتنشن", section "The problem of standard
+  attention" (the only formula the pages print), with 1/sqrt(d_k) passed in as
+  ``scale``.  The mask is the causal one ("masking" is one of the fused steps,
+  same page, section "Fusion of the operations into one CUDA kernel"):
+  key j is visible to query i iff j <= i, and hidden scores are -inf.
+* Logsumexp ``L_i = ln sum_j exp(S_ij)`` of the scaled, masked scores, natural
+  log.  The pages keep a running maximum and a running sum of exponentials per
+  row (same page, section "Online softmax"); L is the pair folded into one
+  number, so the backward pass can rebuild P as exp(S - L).
+* Backward with upstream gradient dO: the derivatives of the same formula,
+  dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic, dS = P o (dP - D),
+  dQ = scale dS K, dK = scale dS^T Q.  The pages state only that the method
+  speeds up training (page "FlashAttention-2 — فلاش أتنشن-2", section
+  "Performance and efficiency"), so a gradient exists; these are the standard
+  chain-rule derivatives of softmax, written out.
+
+Pins (tests/test_oracle.py): rows of P sum to 1; a blockwise online softmax
+written independently in the tests equals this two-pass softmax; constant V
+rows reproduce the constant; causal row 0 attends to key 0 only; Q = 0 gives
+uniform attention with L = ln(#visible keys); N = 1; hand-derived two-token
+examples; torch float64 softmax + autograd as a library cross-check; central
+finite differences for the backward pass; and the identity
+sum_c dO o O = sum_j P o dP.  Every function below is pinned by at least one.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "scores",
+    "probabilities",
+    "attention_forward",
+    "attention_backward",
+    "forward_rows",
+    "head_backward_rowwise",
+]
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of the stored values (fp16/bf16/fp32 tensors or arrays) to float64."""
+    if hasattr(x, "detach"):  # a torch tensor: widen through float32, which is exact for 16-bit types
+        x = x.detach().cpu().float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def scores(q_h, k_h, scale: float, causal: bool, rows=None) -> np.ndarray:
+    """S = scale * q k^T for one head, with -inf where the causal mask hides key j from query i.
+
+    ``rows`` selects query rows (their absolute indices decide the mask).
+    """
+    q_h = _f64(q_h)
+    k_h = _f64(k_h)
+    idx = np.arange(q_h.shape[0]) if rows is None else np.asarray(rows)
+    S = float(scale) * (q_h[idx] @ k_h.T)
+    if causal:
+        keys = np.arange(k_h.shape[0])
+        S = np.where(keys[None, :] > idx[:, None], -np.inf, S)
+    return S
+
+
+def probabilities(S: np.ndarray):
+    """Row softmax of S by the two-pass textbook form; returns (P, L) with L the natural logsumexp."""
+    M = S.max(axis=1, keepdims=True)
+    E = np.exp(S - M)
+    l = E.sum(axis=1, keepdims=True)
+    P = E / l
+    L = (M + np.log(l))[:, 0]
+    return P, L
+
+
+def attention_forward(q, k, v, scale: float, causal: bool):
+    """O [B,H,N,d] and L [B,H,N] in float64, one head at a time, S and P materialised."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    O = np.empty((B, H, N, d))
+    L = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            P, Lh = probabilities(scores(q[b, h], k[b, h], scale, causal))
+            O[b, h] = P @ v[b, h]
+            L[b, h] = Lh
+    return O, L
+
+
+def _head_backward(q_h, k_h, v_h, do_h, scale, causal):
+    P, _ = probabilities(scores(q_h, k_h, scale, causal))
+    O = P @ v_h
+    dV = P.T @ do_h
+    dP = do_h @ v_h.T
+    D = (do_h * O).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    dQ = scale * (dS @ k_h)
+    dK = scale * (dS.T @ q_h)
+    return dQ, dK, dV, D
+
+
+def attention_backward(q, k, v, dout, scale: float, causal: bool):
+    """dQ, dK, dV [B,H,N,d] and D [B,H,N] in float64 for the loss sum(O o dout)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, N, d = q.shape
+    dQ = np.empty_like(q)
+    dK = np.empty_like(k)
+    dV = np.empty_like(v)
+    D = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            dQ[b, h], dK[b, h], dV[b, h], D[b, h] = _head_backward(
+                q[b, h], k[b, h], v[b, h], dout[b, h], float(scale), causal)
+    return dQ, dK, dV, D
+
+
+def forward_rows(q_h, k_h, v_h, scale: float, causal: bool, rows):
+    """O and L of selected query rows of one head: the definition applied row by row.
+
+    Each row's softmax depends on that row's scores only, so evaluating a subset
+    of rows is the same computation as the full forward pass restricted to them.
+    """
+    v_h = _f64(v_h)
+    P, L = probabilities(scores(q_h, k_h, scale, causal, rows=rows))
+    return P @ v_h, L
+
+
+def head_backward_rowwise(q_h, k_h, v_h, do_h, scale: float, causal: bool, chunk: int = 1024):
+    """dQ, dK, dV, D of one head, evaluating the definition over chunks of query rows.
+
+    For long sequences the N x N matrices of one head do not fit comfortably in
+    host memory, so rows are taken ``chunk`` at a time: every row's P, dP and dS
+    come from the definition for that row alone, dQ rows are written directly,
+    and the dK, dV sums over rows are accumulated chunk after chunk.
+    """
+    q_h, k_h, v_h, do_h = _f64(q_h), _f64(k_h), _f64(v_h), _f64(do_h)
+    N, d = q_h.shape
+    dQ = np.empty_like(q_h)
+    dK = np.zeros_like(k_h)
+    dV = np.zeros_like(v_h)
+    D = np.empty(N)
+    for r0 in range(0, N, chunk):
+        rows = np.arange(r0, min(N, r0 + chunk))
+        P, _ = probabilities(scores(q_h, k_h, scale, causal, rows=rows))
+        O = P @ v_h
+        dP = do_h[rows] @ v_h.T
+        Dr = (do_h[rows] * O).sum(axis=1)
+        dS = P * (dP - Dr[:, None])
+        dQ[rows] = scale * (dS @ k_h)
+        dK += scale * (dS.T @ q_h[rows])
+        dV += P.T @ do_h[rows]
+        D[rows] = Dr
+    return dQ, dK, dV, D
