@@ -1,0 +1,356 @@
+#!/usr/bin/env python3
+"""Attention throughput on GB300: one step = forward + backward (D pre-pass, main
+backward kernel, dQ conversion) of exact causal attention over one batch.
+
+Workload (default): B=2, H=16, N=8192, d=128, bf16, causal, Q/K/V = 0.5*N(0,1),
+dO = N(0,1) (seeded, synthetic).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+FLOP accounting: forward 4*B*H*N^2*d, backward 2.5x that, both halved under the
+causal mask.  ``value`` is forward+backward TFLOP/s with inputs resident in
+device memory; ``e2e`` is the same metric through the C-ABI with host buffers
+(pinned host->device copies of Q, K, V, dO and device->host copies of O, L, dQ,
+dK, dV inside the timed region).  L2 is flushed (a 256 MB write) before every
+timed step.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd (bf16, causal/non-causal) and % of GB300 peak"
+UNIT = "TFLOP/s"
+
+
+def attention_flops(w, backward=True):
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    if w.causal:
+        f /= 2
+    return f * (3.5 if backward else 1.0)
+
+
+def load_peaks():
+    p = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def profile_traffic(kernel_tag):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if the kernel
+    source has not changed since the capture (else None)."""
+    import hashlib
+
+    summ = os.path.join(HERE, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(summ):
+        return None
+    fields = {}
+    for line in open(summ):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    src = fields.get("source")
+    want = fields.get("source_sha256")
+    tb = fields.get("traffic_bytes_per_launch")
+    if not (src and want and tb):
+        return None
+    path = os.path.join(HERE, src)
+    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != want:
+        return None
+    try:
+        return float(tb)
+    except ValueError:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(x, world, device):
+    """Max of a float over ranks (control plane only; the attention work exchanges nothing)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(w, heads=1):
+    """Time the oracle (as it stands) on `heads` heads of the workload, forward + backward."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_37_gb300.synth import make_inputs
+
+    q, k, v, do = make_inputs(w.with_(B=1, H=heads), with_dout=True)
+    t0 = time.perf_counter()
+    for h in range(heads):
+        oracle.forward_rows(q[0, h], k[0, h], v[0, h], w.scale, w.causal, np.arange(w.N))
+        oracle.head_backward_rowwise(q[0, h], k[0, h], v[0, h], do[0, h], w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    flops = attention_flops(w.with_(B=1, H=heads))
+    return flops / dt / 1e12, dt
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, 1)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, dt = cpu_oracle_sample(w, 1)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.mean(vals)
+    sample = f"1 of {w.B * w.H} heads per step, forward + backward, fp64 numpy (row chunks of 1024)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_B2_H16_N8192_d128_bf16_causal")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from exact_attention_37_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+
+    import exact_attention_37_gb300 as fa
+    from exact_attention_37_gb300 import build
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    fa.load()
+
+    q, k, v, do = synth.make_inputs(w, with_dout=True)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    B, H, N, d = qd.shape
+    od = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
+        fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.fa_check_device_status()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            e0, e1, e2, e3, e4 = ev[i]
+            fa.fa_bwd_set_main_kernel_events(e2, e3)
+            e0.record(stream)
+            fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
+            e1.record(stream)
+            fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
+            e4.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    fa.fa_bwd_set_main_kernel_events(None, None)
+    fa.fa_check_device_status()
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
+    bwd_main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = reduce_max(sum(step_ms), world, dev)
+    ms_per_step = total_ms / K
+
+    flops_step = attention_flops(w)
+    flops_fwd = attention_flops(w, backward=False)
+    value = world * flops_step * K / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers
+    pin = lambda t: t.pin_memory()
+    qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
+    oh, dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v, q))
+    lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh, doh))
+    d2h = sum(x.numel() * x.element_size() for x in (oh, lseh, dqh, dkh, dvh))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(K):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for hsrc, dst in ((qh, qd), (kh, kd), (vh, vd), (doh, dod)):
+            dst.copy_(hsrc, non_blocking=True)
+        step()
+        for dsrc, hdst in ((od, oh), (lse, lseh), (dq, dqh), (dk, dkh), (dv, dvh)):
+            hdst.copy_(dsrc, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    fa.fa_check_device_status()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
+    e2e_value = world * flops_step * K / (e2e_ms / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_main_avg = statistics.mean(bwd_main_ms)
+    flops_bwd = flops_step - flops_fwd
+    if bwd_main_avg >= fwd_avg:
+        dom, dom_ms, dom_flops, tag = "fa_bwd_kernel", bwd_main_avg, flops_bwd, "fa_bwd_kernel_long"
+    else:
+        dom, dom_ms, dom_flops, tag = "fa_fwd_kernel", fwd_avg, flops_fwd, "fa_fwd_kernel_long"
+    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    fwd_tflops = flops_fwd / (fwd_avg / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profile_traffic(tag),
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = 2
+        cv, cdt = cpu_oracle_sample(w, heads)
+        cpu = {"value": cv, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} heads, forward + backward, fp64 numpy, {cdt:.1f} s"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                       "step": "fwd + bwd (pre, main, dq convert)", "l2": "256 MB flush write before every step",
+                       "parallelism": f"replicas x{world}"},
+            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"])},
+            "bwd": {"tflops": flops_bwd / (statistics.mean(bwd_ms) / 1e3) / 1e12, "ms": statistics.mean(bwd_ms),
+                    "main_kernel_ms": bwd_main_avg},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * K,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

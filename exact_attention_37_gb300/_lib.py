@@ -1,0 +1,148 @@
+"""ctypes binding of the C ABI in include/fa_attention.h -- argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of ``libfa_attention.so``;
+this module turns torch tensors into pointers, sizes and the current stream,
+and turns status codes into exceptions.  There is no fallback: if the library
+is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfa_attention.so")
+
+FA_OK = 0
+STATUS = {
+    0: "FA_OK",
+    1: "FA_ERR_INVALID_ARG",
+    2: "FA_ERR_UNSUPPORTED",
+    3: "FA_ERR_MISALIGNED",
+    4: "FA_ERR_WORKSPACE",
+    5: "FA_ERR_CUDA",
+    6: "FA_ERR_DEVICE_TIMEOUT",
+}
+FA_FP16, FA_BF16 = 0, 1
+
+# Every symbol the header declares, with (restype, argtypes).
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_check_device_status": (_i, [_vp]),
+    "fa_last_device_error_bits": (ctypes.c_uint32, []),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_bwd_set_main_kernel_events": (None, [_vp, _vp]),
+    "fa_version": (ctypes.c_uint32, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (once) and declare its signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FaError(f"loading {os.path.basename(path)} (not built; run exact_attention_37_gb300.build)", -1)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(where: str, code: int):
+    if code != FA_OK:
+        raise FaError(where, code)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp16 or bf16 only")
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):
+    """O and L into caller-owned ``o`` [B,H,N,d] and ``lse`` [B,H,N] fp32 (all CUDA, contiguous)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    for t in (q, k, v, o, lse):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    code = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+                      _dtype_code(q), _stream(stream))
+    _check("fa_fwd", code)
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None):
+    """dQ, dK, dV into caller-owned tensors; ``workspace`` is a CUDA uint8 tensor of at least
+    fa_bwd_workspace_size bytes."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    for t in (q, k, v, o, dout, lse, dq, dk, dv):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    code = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                      _ptr(workspace), ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q),
+                      _stream(stream))
+    _check("fa_bwd", code)
+
+
+def fa_check_device_status(stream=None):
+    """Synchronize and raise FaError(FA_ERR_DEVICE_TIMEOUT) if a kernel gave up on a wait."""
+    _check("fa_check_device_status", load().fa_check_device_status(_stream(stream)))
+
+
+def fa_bwd_set_main_kernel_events(before=None, after=None):
+    """Record torch.cuda.Event ``before``/``after`` around the main backward kernel (None, None to stop)."""
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
+    load().fa_bwd_set_main_kernel_events(b, a)
+
+
+def fa_status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> int:
+    return int(load().fa_version())

@@ -1,0 +1,227 @@
+// C-ABI entry points of the exact-attention library (declared in include/fa_attention.h).
+//
+// This layer validates arguments on the host (nothing is launched for a bad
+// call), encodes the TMA descriptors of the [B*H, N, d] tensors, lays out the
+// backward workspace, and owns the device error word that the kernels' bounded
+// waits write.  It allocates no device memory.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa_attention.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// Device word the kernels set when a bounded wait gives up (one per device that loads the library).
+__device__ uint32_t g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t g_last_bits = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Address of the error word on the current device (looked up once per device).
+uint32_t* error_word_ptr() {
+  static uint32_t* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by both passes.  Returns FA_OK or the first problem found.
+fa_status check_common(int B, int H, int N, int d, float scale, int dtype) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  // grid size and 32-bit index limits of the kernels
+  if (BH > (1LL << 24) || N > (1 << 28)) return FA_ERR_UNSUPPORTED;
+  const long long fwd_ctas = BH * ((N + 127) / 128);
+  if (fwd_ctas * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
+  return FA_OK;
+}
+
+// TMA descriptor of a [BH, N, d] 16-bit tensor read or written in boxes of
+// 64 columns (128 B, 128-byte swizzle) x `box_rows` rows of one head.
+bool make_map(CUtensorMap* m, const void* ptr, long long BH, int N, int d, bool bf16, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int bwd_query_rows(int d);
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+  if (st != FA_OK) return st;
+  if ((long long)B * H * N == 0) return FA_OK;  // empty problem
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  if ((st = check_device()) != FA_OK) return st;
+  const bool bf16 = dtype == FA_BF16;
+  const long long BH = (long long)B * H;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, q, BH, N, d, bf16, 128) || !make_map(&mk, k, BH, N, d, bf16, 128) ||
+      !make_map(&mv, v, BH, N, d, bf16, 128) || !make_map(&mo, o, BH, N, d, bf16, 128))
+    return FA_ERR_CUDA;
+  FwdArgs a{};
+  a.lse = lse;
+  a.N = N;
+  a.BH = (int)BH;
+  const int rows = fwd_rows_per_cta(d);
+  a.num_qblocks = (N + rows - 1) / rows;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.err = error_word_ptr();
+  if (!a.err) return FA_ERR_CUDA;
+  cudaError_t e = launch_fwd(d, bf16, mq, mk, mv, mo, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_common(B, H, N, d, 1.f, FA_FP16) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  if (rows == 0) return 0;
+  return round_up(rows * d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+  if (st != FA_OK) return st;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+  if ((st = check_device()) != FA_OK) return st;
+  const bool bf16 = dtype == FA_BF16;
+  const long long BH = (long long)B * H;
+  const int bm = bwd_query_rows(d);
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, q, BH, N, d, bf16, bm) || !make_map(&mk, k, BH, N, d, bf16, 128) ||
+      !make_map(&mv, v, BH, N, d, bf16, 128) || !make_map(&mdo, dout, BH, N, d, bf16, bm))
+    return FA_ERR_CUDA;
+  const size_t rows = (size_t)BH * N;
+  BwdArgs a{};
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq_acc = static_cast<float*>(workspace);
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * d * sizeof(float), 256));
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.N = N;
+  a.d = d;
+  a.BH = (int)BH;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.err = error_word_ptr();
+  if (!a.err) return FA_ERR_CUDA;
+  cudaError_t e = launch_bwd(d, bf16, mq, mk, mv, mdo, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_check_device_status(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_error_word, sizeof(bits)) != cudaSuccess) return FA_ERR_CUDA;
+  g_last_bits = bits;
+  if (bits != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+uint32_t fa_last_device_error_bits(void) { return g_last_bits; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+void fa_bwd_set_main_kernel_events(void* before, void* after) {
+  g_bwd_main_before = static_cast<cudaEvent_t>(before);
+  g_bwd_main_after = static_cast<cudaEvent_t>(after);
+}
+
+uint32_t fa_version(void) { return (1u << 16) | 0u; }
+
+}  // extern "C"

@@ -1,0 +1,532 @@
+// Backward pass of exact attention for sm_103a.
+//
+// The pages say the method serves training (page "FlashAttention-2 —
+// فلاش أتنشن-2", section "Performance and efficiency") and that no N x N matrix
+// is kept in device memory (page "FlashAttention — فلاش أتنشن", section
+// "Tiling and block processing"); the backward pass therefore rebuilds the
+// probabilities block by block from Q, K and the forward pass's logsumexp L:
+//
+//   D_i  = sum_c dO_ic O_ic                       (pre-pass, one value per row)
+//   P    = exp(scale * q_i.k_j - L_i)             (recomputed, never stored globally)
+//   dV_j = sum_i P_ij dO_i
+//   dS   = P o (dO_i . v_j - D_i)
+//   dK_j = scale * sum_i dS_ij q_i
+//   dQ_i = scale * sum_j dS_ij k_j                (fp32 accumulator, atomics)
+//
+// Work is split over (batch*head, key block of 128 keys) -- the key-block
+// parallelism of page "FlashAttention-2 — فلاش أتنشن-2", section "Technical
+// architecture", item 2 -- and, for d = 256, over two 128-column halves of the
+// gradients.  Each CTA keeps K_j and V_j in shared memory and the dK_j, dV_j
+// accumulators in TMEM, and streams the query blocks it needs (under the causal
+// mask only those at or after the diagonal).
+//
+// Everything is computed transposed, keys on TMEM lanes: S^T = K_j Q_i^T and
+// dP^T = V_j dO_i^T give every softmax thread one key row, so P^T and dS^T can
+// be written as the K-major A operands of dV += P^T dO and dK += dS^T Q.  dQ
+// uses the same dS^T tile read MN-major: dQ_i = dS K_j (keys on the K side) for
+// 128-row query blocks, or dQ_i^T = K_j^T dS^T for 64-row query blocks so that
+// the accumulator keeps M = 128.
+//
+// Warp roles: warps 0-3 turn S^T and dP^T into P^T and dS^T; warps 4-7 drain
+// dQ from TMEM into the fp32 accumulator and write dK, dV at the end; warp 8
+// issues TMA loads; warp 9 issues the tcgen05 MMAs.
+#include <algorithm>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBN = 128;   // keys per CTA (= TMEM lanes)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// D, DH: head dim and gradient columns per CTA; BM: query rows per block;
+// DQT: compute dQ^T (M = DH) instead of dQ (M = BM); STG: Q/dO pipeline depth.
+template <int D, int DH, int BM, bool DQT, int STG>
+struct BwdLayout {
+  static constexpr uint32_t kKVPanel = kBN * 128;                 // 128 key rows x 128 B
+  static constexpr uint32_t kQPanel = BM * 128;                   // BM query rows x 128 B
+  static constexpr uint32_t kKVTile = (D / 64) * kKVPanel;
+  static constexpr uint32_t kQTile = (D / 64) * kQPanel;
+  static constexpr uint32_t kPdsPanel = kBN * 128;                // 128 key rows x 64 queries
+  static constexpr uint32_t kPdsTile = (BM / 64) * kPdsPanel;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kKVTile;
+  static constexpr uint32_t kQ = kV + kKVTile;                    // STG stages of (Q, dO)
+  static constexpr uint32_t kPt = kQ + STG * 2 * kQTile;
+  static constexpr uint32_t kDSt = kPt + kPdsTile;
+  static constexpr uint32_t kLD = kDSt + kPdsTile;                // 2 buffers x (L, D) x BM floats
+  static constexpr uint32_t kBar = kLD + 2 * 2 * BM * 4;
+  static constexpr int kKVFull = 0;
+  static constexpr int kQFull = 1;
+  static constexpr int kQEmpty = kQFull + STG;
+  static constexpr int kSFull = kQEmpty + STG;
+  static constexpr int kPdsFull = kSFull + 1;
+  static constexpr int kGrads = kPdsFull + 1;
+  static constexpr int kDqFree = kGrads + 1;
+  static constexpr int kDrain = kDqFree + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kTmemSlot + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = BM;
+  static constexpr uint32_t kColDV = 2 * BM;
+  static constexpr uint32_t kColDK = 2 * BM + DH;
+  static constexpr uint32_t kColDQ = 2 * BM + 2 * DH;
+  static constexpr uint32_t kDqCols = DQT ? BM : DH;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColDQ + kDqCols <= 512, "TMEM budget");
+  static_assert(kBytes + 1024 <= 232448, "shared memory budget");
+  static_assert(!DQT || DH == 128, "dQ^T needs M = 128");
+  static_assert(DQT || BM == 128, "dQ needs M = 128");
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red_add(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+__device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int D, int DH, int BM, bool DQT, int STG, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdArgs args) {
+  using L = BwdLayout<D, DH, BM, DQT, STG>;
+  constexpr int kHalves = D / DH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  auto sQ = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s; };
+  auto sDO = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s + L::kQTile; };
+  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sPt = sbase + L::kPt, sDSt = sbase + L::kDSt;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+
+  // Work tile: key block kb (lowest first: under the causal mask it has the most query blocks).
+  const int tiles_per_kb = args.BH * kHalves;
+  const int kb = (int)(blockIdx.x / tiles_per_kb);
+  const int rem = (int)(blockIdx.x % tiles_per_kb);
+  const int bh = rem / kHalves;
+  const int half = rem % kHalves;
+  const int key0 = kb * kBN;
+  const int nqb = (N + BM - 1) / BM;
+  const int i_begin = args.causal ? key0 / BM : 0;
+  const int nit = nqb - i_begin;  // query blocks this CTA visits (>= 1)
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kKVFull), 1);
+    for (int s = 0; s < STG; ++s) {
+      mbar_init(bar(L::kQFull + s), 1);
+      mbar_init(bar(L::kQEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kPdsFull), 128);
+    mbar_init(bar(L::kGrads), 1);
+    mbar_init(bar(L::kDqFree), 128);
+    mbar_init(bar(L::kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(sbase + L::kTmemSlot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(L::kKVFull), 2 * L::kKVTile);
+#pragma unroll
+      for (int p = 0; p < D / 64; ++p) {
+        tma_load_3d(sK + p * L::kKVPanel, &tm_k, bar(L::kKVFull), 64 * p, key0, bh);
+        tma_load_3d(sV + p * L::kKVPanel, &tm_v, bar(L::kKVFull), 64 * p, key0, bh);
+      }
+      for (int it = 0; it < nit; ++it) {
+        const int s = it % STG, u = it / STG;
+        if (u > 0 && !mbar_wait(bar(L::kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(L::kQFull + s), 2 * L::kQTile);
+        const int q0 = (i_begin + it) * BM;
+#pragma unroll
+        for (int p = 0; p < D / 64; ++p) {
+          tma_load_3d(sQ(s) + p * L::kQPanel, &tm_q, bar(L::kQFull + s), 64 * p, q0, bh);
+          tma_load_3d(sDO(s) + p * L::kQPanel, &tm_do, bar(L::kQFull + s), 64 * p, q0, bh);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_f16(BF16, kBN, BM, false, false);     // S^T, dP^T: M=128 keys, N=BM
+      constexpr uint32_t kIdG = make_idesc_f16(BF16, kBN, DH, false, true);      // dV, dK: M=128 keys, N=DH
+      constexpr uint32_t kIdQ = DQT ? make_idesc_f16(BF16, DH, BM, true, true)   // dQ^T: M=DH, N=BM, A=K^T
+                                    : make_idesc_f16(BF16, BM, DH, true, true);  // dQ: M=BM, N=DH, A=dS
+      const uint32_t hp = (uint32_t)(half * (DH / 64));  // first 64-column panel of this CTA's half
+      auto issue_sdp = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kKVPanel + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
+          mma_ss(tmem + L::kColS, make_sdesc_sw128(sK + a_off, 16, 1024), make_sdesc_sw128(sQ(s) + b_off, 16, 1024),
+                 kIdS, kk > 0);
+          mma_ss(tmem + L::kColDP, make_sdesc_sw128(sV + a_off, 16, 1024),
+                 make_sdesc_sw128(sDO(s) + b_off, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      auto issue_grads = [&](int s, int it) {
+        // dV += P^T dO, dK += dS^T Q: A K-major over the BM queries, B MN-major (DH columns).
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kPdsPanel + (kk & 3) * 32;
+          const uint32_t b_off = hp * L::kQPanel + kk * 2048;
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          mma_ss(tmem + L::kColDV, make_sdesc_sw128(sPt + a_off, 16, 1024),
+                 make_sdesc_sw128(sDO(s) + b_off, L::kQPanel, 1024), kIdG, acc);
+          mma_ss(tmem + L::kColDK, make_sdesc_sw128(sDSt + a_off, 16, 1024),
+                 make_sdesc_sw128(sQ(s) + b_off, L::kQPanel, 1024), kIdG, acc);
+        }
+        // dQ (or dQ^T) over the 128 keys of this block; both operands MN-major.
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t k_off = hp * L::kKVPanel + kk * 2048;
+          const uint32_t ds_off = kk * 2048;
+          if constexpr (DQT) {
+            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024),
+                   make_sdesc_sw128(sDSt + ds_off, L::kPdsPanel, 1024), kIdQ, kk > 0);
+          } else {
+            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sDSt + ds_off, L::kPdsPanel, 1024),
+                   make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024), kIdQ, kk > 0);
+          }
+        }
+      };
+      bool ok = mbar_wait(bar(L::kKVFull), 0, args.err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait(bar(L::kQFull + 0), 0, args.err, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0);
+        mma_commit(bar(L::kSFull));
+      }
+      for (int it = 0; ok && it < nit; ++it) {
+        const int s = it % STG;
+        ok = mbar_wait(bar(L::kPdsFull), it & 1, args.err, kErrTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        // Scores of the next block first, so the softmax warps can start on them
+        // while the tensor cores compute this block's gradients.
+        if (it + 1 < nit) {
+          const int s1 = (it + 1) % STG;
+          ok = mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sdp(s1);
+          mma_commit(bar(L::kSFull));
+        }
+        if (it > 0) {
+          ok = mbar_wait(bar(L::kDqFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_grads(s, it);
+        mma_commit(bar(L::kGrads));
+        mma_commit(bar(L::kQEmpty + s));
+      }
+      mma_commit(bar(L::kDrain));
+      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T and dS^T
+    const int r = (warp << 5) + lane;  // key row inside the block == TMEM lane
+    const int key = key0 + r;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c = args.scale_log2;
+    float* sL = reinterpret_cast<float*>(smem + L::kLD);  // [2][2][BM]: (L*log2e, D) per buffer
+    const size_t row_base = (size_t)bh * N;
+    for (int it = 0; it < nit; ++it) {
+      const int i = i_begin + it;
+      const int q0 = i * BM;
+      float* bufL = sL + (it & 1) * 2 * BM;
+      float* bufD = bufL + BM;
+      if (r < BM) {
+        const int q = q0 + r;
+        bufL[r] = (q < N) ? args.lse[row_base + q] * kLog2e : INFINITY;  // rows past N get P = 0
+        bufD[r] = (q < N) ? args.delta[row_base + q] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      if (!mbar_wait(bar(L::kSFull), it & 1, args.err, kErrTimeoutMma)) break;
+      tc_fence_after();
+      const bool diag = args.causal && (key0 + kBN - 1 > q0);  // some key of the block is after some query
+      uint32_t pw[BM / 2], dw[BM / 2];
+      bool ok = true;
+      if constexpr (BM == 128) {
+        // Wide blocks: free the P^T / dS^T tiles first, then write chunk by chunk.
+        if (it > 0) {
+          ok = mbar_wait(bar(L::kGrads), (it - 1) & 1, args.err, kErrTimeoutMma);
+          tc_fence_after();
+        }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int ch = 0; ch < BM / 32; ++ch) {
+        uint32_t sv[32], dv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + 32 * ch, sv);
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + 32 * ch, dv);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(dv);
+        float p[32], ds[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = 32 * ch + e;
+          float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -bufL[col]));
+          if (diag && key > q0 + col) pe = 0.f;
+          p[e] = pe;
+          ds[e] = pe * (__uint_as_float(dv[e]) - bufD[col]);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pw[(ch * 32) / 2 + e] = pack2<BF16>(p[2 * e], p[2 * e + 1]);
+          dw[(ch * 32) / 2 + e] = pack2<BF16>(ds[2 * e], ds[2 * e + 1]);
+        }
+        if constexpr (BM == 128) {
+          // chunk ch covers 16-byte chunks 4ch..4ch+3 of the row
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int chunk = ch * 4 + k4;
+            const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
+            const int w = (ch * 32) / 2 + 4 * k4;
+            st_shared_v4(sPt + off, pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
+            st_shared_v4(sDSt + off, dw[w], dw[w + 1], dw[w + 2], dw[w + 3]);
+          }
+        }
+      }
+      tc_fence_before();  // done reading S^T and dP^T from TMEM
+      if constexpr (BM != 128) {
+        if (it > 0) {
+          if (!mbar_wait(bar(L::kGrads), (it - 1) & 1, args.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int chunk = 0; chunk < BM / 8; ++chunk) {
+          const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
+          st_shared_v4(sPt + off, pw[4 * chunk], pw[4 * chunk + 1], pw[4 * chunk + 2], pw[4 * chunk + 3]);
+          st_shared_v4(sDSt + off, dw[4 * chunk], dw[4 * chunk + 1], dw[4 * chunk + 2], dw[4 * chunk + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::kPdsFull));
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+    const int wq = warp - 4;
+    const int r = (wq << 5) + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    float* dq_acc = args.dq_acc + (size_t)bh * N * D;
+    bool ok = true;
+    for (int it = 0; it < nit; ++it) {
+      const int q0 = (i_begin + it) * BM;
+      ok = mbar_wait(bar(L::kGrads), it & 1, args.err, kErrTimeoutMma);
+      if (!ok) break;
+      tc_fence_after();
+      constexpr int kCh = L::kDqCols / 32;
+      uint32_t v[kCh][32];
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) tmem_ld_32x32b_x32(tmem + lane_base + L::kColDQ + 32 * ch, v[ch]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) reg_fence32(v[ch]);
+      tc_fence_before();
+      mbar_arrive(bar(L::kDqFree));
+      if constexpr (DQT) {
+        // lane r holds dQ^T row r: column half*DH + r of query rows q0 .. q0+BM-1
+        const int col = half * DH + r;
+#pragma unroll
+        for (int ch = 0; ch < kCh; ++ch)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int q = q0 + 32 * ch + e;
+            if (q < N) red_add(dq_acc + (size_t)q * D + col, __uint_as_float(v[ch][e]));
+          }
+      } else {
+        // lane r holds dQ row q0 + r, columns half*DH .. half*DH+DH-1
+        const int q = q0 + r;
+        if (q < N) {
+          float* dst = dq_acc + (size_t)q * D + half * DH;
+#pragma unroll
+          for (int ch = 0; ch < kCh; ++ch)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4(dst + 32 * ch + e, __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]),
+                         __uint_as_float(v[ch][e + 2]), __uint_as_float(v[ch][e + 3]));
+        }
+      }
+    }
+    if (ok) {
+      // Final gradients of this key block; lane r holds key row key0 + r.
+      const int key = key0 + r;
+      const size_t out_row = ((size_t)bh * N + key) * D + half * DH;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? L::kColDV : L::kColDK;
+        const float mul = which == 0 ? 1.f : args.scale;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + out_row;
+#pragma unroll 1
+        for (int ch = 0; ch < DH / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + col0 + 32 * ch, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (key < N) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+              st_global_v4(dst + 32 * ch + e,
+                           pack2<BF16>(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul),
+                           pack2<BF16>(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul),
+                           pack2<BF16>(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul),
+                           pack2<BF16>(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// D_i = sum_c dO_ic O_ic per row, and the fp32 dQ accumulator set to zero.
+// One warp per row, grid-stride; each lane handles D/32 consecutive elements.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, long long rows) {
+  constexpr int kPer = D / 32;  // 2, 4 or 8 elements per lane
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const uint16_t* o = reinterpret_cast<const uint16_t*>(args.o);
+  const uint16_t* g = reinterpret_cast<const uint16_t*>(args.dout);
+  for (long long row = warp0; row < rows; row += nwarps) {
+    const size_t base = (size_t)row * D + lane * kPer;
+    float acc = 0.f;
+    uint16_t ov[kPer], gv[kPer];
+    if constexpr (kPer == 8) {
+      *reinterpret_cast<uint4*>(ov) = *reinterpret_cast<const uint4*>(o + base);
+      *reinterpret_cast<uint4*>(gv) = *reinterpret_cast<const uint4*>(g + base);
+    } else if constexpr (kPer == 4) {
+      *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(o + base);
+      *reinterpret_cast<uint2*>(gv) = *reinterpret_cast<const uint2*>(g + base);
+    } else {
+      *reinterpret_cast<uint32_t*>(ov) = *reinterpret_cast<const uint32_t*>(o + base);
+      *reinterpret_cast<uint32_t*>(gv) = *reinterpret_cast<const uint32_t*>(g + base);
+    }
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      acc = fmaf(widen16<BF16>(ov[e]), widen16<BF16>(gv[e]), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) args.delta[row] = acc;
+    float* z = args.dq_acc + base;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) *reinterpret_cast<float2*>(z + e) = make_float2(0.f, 0.f);
+  }
+}
+
+// dQ = scale * dQ_acc rounded to 16 bits; 8 elements per thread, grid-stride.
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const BwdArgs args, long long n8) {
+  const float4* src = reinterpret_cast<const float4*>(args.dq_acc);
+  uint4* dst = reinterpret_cast<uint4*>(args.dq);
+  const float s = args.scale;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const float4 a = src[2 * i], b = src[2 * i + 1];
+    dst[i] = make_uint4(pack2<BF16>(a.x * s, a.y * s), pack2<BF16>(a.z * s, a.w * s), pack2<BF16>(b.x * s, b.y * s),
+                        pack2<BF16>(b.z * s, b.w * s));
+  }
+}
+
+template <int D, int DH, int BM, bool DQT, int STG, bool BF16>
+cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                         const BwdArgs& a, cudaStream_t stream) {
+  using L = BwdLayout<D, DH, BM, DQT, STG>;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows = (long long)a.BH * a.N;
+  // 1) D and zeroed dQ accumulator
+  {
+    const long long want = (rows + 7) / 8;
+    const int grid = (int)std::min<long long>(want, (long long)sms * 16);
+    fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(a, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2) main kernel
+  {
+    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
+    if (e != cudaSuccess) return e;
+    const long long nkb = (a.N + kBN - 1) / kBN;
+    const long long grid = nkb * a.BH * (D / DH);
+    if (g_bwd_main_before && g_bwd_main_after) cudaEventRecord(g_bwd_main_before, stream);
+    kern<<<(unsigned)grid, 320, L::kAlloc, stream>>>(q, k, v, dout, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (g_bwd_main_before && g_bwd_main_after) cudaEventRecord(g_bwd_main_after, stream);
+  }
+  // 3) dQ conversion
+  {
+    const long long n8 = rows * D / 8;
+    const int grid = (int)std::min<long long>((n8 + 255) / 256, (long long)sms * 16);
+    fa_bwd_dq_convert_kernel<BF16><<<grid, 256, 0, stream>>>(a, n8);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaEvent_t g_bwd_main_before = nullptr;
+cudaEvent_t g_bwd_main_after = nullptr;
+
+int bwd_query_rows(int d) { return d == 64 ? 128 : 64; }
+
+cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
+  switch (d) {
+    case 64:
+      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<64, 64, 128, false, 3, false>(q, k, v, dout, a, stream);
+    case 128:
+      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<128, 128, 64, true, 3, false>(q, k, v, dout, a, stream);
+    case 256:
+      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<256, 128, 64, true, 1, false>(q, k, v, dout, a, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

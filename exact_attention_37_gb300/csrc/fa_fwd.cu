@@ -1,0 +1,423 @@
+// Forward pass of exact attention for sm_103a: O = softmax(Q K^T * scale + mask) V and
+// the per-row logsumexp L, in one fused kernel.
+//
+// The method is the one of the page "FlashAttention — فلاش أتنشن": Q, K and V are
+// split into tiles held on chip (section "Tiling and block processing"), every
+// query row keeps a running maximum and a running sum of exponentials that are
+// updated block by block and give the exact softmax (section "Online softmax"),
+// and the matrix products, the mask, the softmax and the product with V happen
+// in one kernel that writes only the final output (section "Fusion of the
+// operations into one CUDA kernel").  Work is split over (batch*head, query
+// block) so that one head spreads over many SMs (page "FlashAttention-2 —
+// فلاش أتنشن-2", section "Technical architecture", item 2).
+//
+// GB300 mapping (one CTA per 128*NQ query rows):
+//   warp 4*NQ     TMA producer: Q sub-tiles once, then K_j / V_j tiles through a
+//                 ring of STAGES shared-memory slots, in the order the MMA warp
+//                 consumes them (K_0, K_1, V_0, K_2, V_1, ...).
+//   warp 4*NQ+1   MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
+//                 O_t += P_t V_j into TMEM, with tcgen05.mma (fp32 accumulate).
+//                 S for block j+1 is issued before P V for block j, so the tensor
+//                 cores work while the softmax warps exponentiate.
+//   warps 4t..4t+3  softmax for query sub-tile t: thread r owns query row r and
+//                 TMEM lane r, so every row reduction stays inside one thread.
+//                 Scores are taken to base 2 with one FMA (scale*log2 e folded in),
+//                 exponentiated with ex2, summed, rounded to 16 bits and written to
+//                 shared memory as the A operand of the P V product.  The row's
+//                 reference maximum only moves when the new maximum exceeds it by
+//                 more than 8 (base 2); otherwise the old one is kept, which leaves
+//                 the result exact (all terms share one reference) and skips the
+//                 rescale of O.  When it moves, the thread rescales its O row in
+//                 TMEM before releasing P.
+//   epilogue      O / l rounded to 16 bits, staged in the dead Q tile, stored by TMA;
+//                 L = m*scale + ln(l) written per row.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;                 // query rows per sub-tile (= TMEM lanes)
+constexpr int kBN = 128;                 // keys per block
+constexpr uint32_t kPanelBytes = 16384;  // 128 rows x 128 B: one 64-column swizzled panel
+
+template <int D, int NQ, int STAGES>
+struct FwdLayout {
+  static constexpr int kPanels = D / 64;
+  static constexpr uint32_t kTileBytes = kPanels * kPanelBytes;  // 128 rows x D 16-bit values
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kRing = kQ + NQ * kTileBytes;
+  static constexpr uint32_t kP = kRing + STAGES * kTileBytes;
+  static constexpr uint32_t kBar = kP + NQ * 2 * kPanelBytes;
+  // barrier indices
+  static constexpr int kQFull = 0;
+  static constexpr int kFull = 1;
+  static constexpr int kEmpty = kFull + STAGES;
+  static constexpr int kSFull = kEmpty + STAGES;
+  static constexpr int kSFree = kSFull + NQ;
+  static constexpr int kPFull = kSFree + NQ;
+  static constexpr int kODone = kPFull + NQ;
+  static constexpr int kDrain = kODone + NQ;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kTmemSlot + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024 B
+  // TMEM columns: S_t at 128*t, O_t after all S tiles.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t s_col(int t) { return 128u * t; }
+  static constexpr uint32_t o_col(int t) { return 128u * NQ + (uint32_t)D * t; }
+  static_assert(128 * NQ + D * NQ <= 512, "TMEM budget");
+  static_assert(kBytes + 1024 <= 232448, "shared memory budget");
+};
+
+template <int D, int NQ, int STAGES, bool BF16>
+__global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdArgs args) {
+  using L = FwdLayout<D, NQ, STAGES>;
+  constexpr int kWarpTma = 4 * NQ;
+  constexpr int kWarpMma = 4 * NQ + 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  auto sQ = [&](int t) -> uint32_t { return sbase + L::kQ + L::kTileBytes * t; };
+  auto sRing = [&](int s) -> uint32_t { return sbase + L::kRing + L::kTileBytes * s; };
+  auto sP = [&](int t) -> uint32_t { return sbase + L::kP + 2u * kPanelBytes * t; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+
+  // Heaviest query blocks first: under the causal mask the last blocks see the most keys.
+  const int qb = args.num_qblocks - 1 - (int)(blockIdx.x / args.BH);
+  const int bh = (int)(blockIdx.x % args.BH);
+  const int row0 = qb * (kBM * NQ);
+
+  // Key blocks each sub-tile visits (0 for a sub-tile entirely past the end).
+  int nblk[NQ];
+  int nb = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int r0 = row0 + kBM * t;
+    if (r0 >= N) {
+      nblk[t] = 0;
+    } else {
+      const int last_key = args.causal ? min(r0 + kBM - 1, N - 1) : N - 1;
+      nblk[t] = last_key / kBN + 1;
+    }
+    nb = max(nb, nblk[t]);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQFull), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(L::kFull + s), 1);
+      mbar_init(bar(L::kEmpty + s), 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(bar(L::kSFull + t), 1);
+      mbar_init(bar(L::kSFree + t), kBM);
+      mbar_init(bar(L::kPFull + t), kBM);
+      mbar_init(bar(L::kODone + t), 1);
+    }
+    mbar_init(bar(L::kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(sbase + L::kTmemSlot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(L::kQFull), NQ * L::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < NQ; ++t)
+#pragma unroll
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_3d(sQ(t) + p * kPanelBytes, &tm_q, bar(L::kQFull), 64 * p, row0 + kBM * t, bh);
+      int e = 0;
+      auto load = [&](const CUtensorMap* m, int j) -> bool {
+        const int s = e % STAGES, u = e / STAGES;
+        if (u > 0 && !mbar_wait(bar(L::kEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) return false;
+        mbar_expect_tx(bar(L::kFull + s), L::kTileBytes);
+#pragma unroll
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * j, bh);
+        ++e;
+        return true;
+      };
+      bool ok = load(&tm_k, 0);
+      for (int j = 0; ok && j < nb; ++j) {
+        if (j + 1 < nb) ok = load(&tm_k, j + 1);
+        if (ok) ok = load(&tm_v, j);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_f16(BF16, kBM, kBN, false, false);
+      constexpr uint32_t kIdPV = make_idesc_f16(BF16, kBM, D, false, true);
+      auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+          mma_ss(tmem + L::s_col(t), make_sdesc_sw128(sQ(t) + off, 16, 1024),
+                 make_sdesc_sw128(sRing(s) + off, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int s, int j) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+          mma_ss(tmem + L::o_col(t), make_sdesc_sw128(sP(t) + a_off, 16, 1024),
+                 make_sdesc_sw128(sRing(s) + kk * 2048, kPanelBytes, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
+      int e = 0;
+      if (ok) {
+        const int s = e % STAGES;
+        ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NQ; ++t)
+            if (nblk[t] > 0) {
+              issue_s(t, s);
+              mma_commit(bar(L::kSFull + t));
+            }
+          mma_commit(bar(L::kEmpty + s));
+          ++e;
+        }
+      }
+      for (int j = 0; ok && j < nb; ++j) {
+        if (j + 1 < nb) {
+          const int s = e % STAGES;
+          ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NQ; ++t)
+            if (ok && j + 1 < nblk[t]) {
+              ok = mbar_wait(bar(L::kSFree + t), j & 1, args.err, kErrTimeoutSoftmax);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, s);
+              mma_commit(bar(L::kSFull + t));
+            }
+          if (!ok) break;
+          mma_commit(bar(L::kEmpty + s));
+          ++e;
+        }
+        const int s = e % STAGES;
+        ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NQ; ++t)
+          if (ok && j < nblk[t]) {
+            ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, s, j);
+            mma_commit(bar(L::kODone + t));
+          }
+        if (!ok) break;
+        mma_commit(bar(L::kEmpty + s));
+        ++e;
+      }
+      // Every MMA must have finished before TMEM can be released.
+      mma_commit(bar(L::kDrain));
+      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;
+    const int r = ((warp & 3) << 5) + lane;  // row inside the sub-tile == TMEM lane
+    const int q_row = row0 + kBM * t + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + L::s_col(t);
+    const uint32_t tO = tmem + lane_base + L::o_col(t);
+    const float c = args.scale_log2;
+    const int key_limit = args.causal ? min(q_row, N - 1) : N - 1;  // last key this row sees
+    float m = -INFINITY;  // reference maximum (raw score units)
+    float l = 0.f;        // running sum of 2^((s - m) c)
+    bool ok = true;
+    const int my_blocks = nblk[t];
+    for (int j = 0; j < my_blocks; ++j) {
+      ok = mbar_wait(bar(L::kSFull + t), j & 1, args.err, kErrTimeoutMma);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(tS + 32 * h, sr[h]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 4; ++h) reg_fence32(sr[h]);
+      tc_fence_before();
+      mbar_arrive(bar(L::kSFree + t));  // S_t may now be overwritten by the next block
+
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+      const int nvalid = key_limit - kBN * j + 1;  // keys kBN*j .. kBN*j+nvalid-1 are visible
+      if (nvalid < kBN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = (i < nvalid) ? s[i] : -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+        mx2 = fmaxf(mx2, s[i + 2]);
+        mx3 = fmaxf(mx3, s[i + 3]);
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+      // Keep the old reference unless the maximum grew by more than 8 (base 2).
+      const float m_use = (m == -INFINITY || (m_new - m) * c > 8.f) ? m_new : m;
+      const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+      const float alpha = ex2_approx(fmaf(m, c, -mc));  // 0 when m = -inf
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; i += 4) {
+        s[i] = ex2_approx(fmaf(s[i], c, -mc));
+        s[i + 1] = ex2_approx(fmaf(s[i + 1], c, -mc));
+        s[i + 2] = ex2_approx(fmaf(s[i + 2], c, -mc));
+        s[i + 3] = ex2_approx(fmaf(s[i + 3], c, -mc));
+        l0 += s[i];
+        l1 += s[i + 1];
+        l2 += s[i + 2];
+        l3 += s[i + 3];
+      }
+      l = l * alpha + ((l0 + l1) + (l2 + l3));
+
+      // P_t and O_t are free once the previous P V product has completed.
+      if (j > 0) {
+        ok = mbar_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int b = h * 64 + cc * 8;
+          st_shared_v4(sP(t) + h * kPanelBytes + sw128_offset(r, cc), pack2<BF16>(s[b], s[b + 1]),
+                       pack2<BF16>(s[b + 2], s[b + 3]), pack2<BF16>(s[b + 4], s[b + 5]),
+                       pack2<BF16>(s[b + 6], s[b + 7]));
+        }
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + 32 * ch, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(tO + 32 * ch, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + t));
+      m = m_use;
+    }
+    if (ok && my_blocks > 0) {
+      ok = mbar_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        if (q_row < N) {
+          args.lse[(size_t)bh * N + q_row] = (l > 0.f) ? m * args.scale + logf(l) : -INFINITY;
+        }
+        // O / l -> 16-bit, staged in the Q tile of this sub-tile (its last use is over).
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + 32 * ch, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int chunk = ch * 4 + k4;  // 16-byte chunk index along the row
+            const int b = k4 * 8;
+            st_shared_v4(sQ(t) + (chunk >> 3) * kPanelBytes + sw128_offset(r, chunk & 7),
+                         pack2<BF16>(__uint_as_float(o[b]) * inv_l, __uint_as_float(o[b + 1]) * inv_l),
+                         pack2<BF16>(__uint_as_float(o[b + 2]) * inv_l, __uint_as_float(o[b + 3]) * inv_l),
+                         pack2<BF16>(__uint_as_float(o[b + 4]) * inv_l, __uint_as_float(o[b + 5]) * inv_l),
+                         pack2<BF16>(__uint_as_float(o[b + 6]) * inv_l, __uint_as_float(o[b + 7]) * inv_l));
+          }
+        }
+        fence_proxy_async_smem();
+      }
+    }
+    // All 128 threads of this sub-tile reach the barrier (ok or not), then one stores.
+    named_bar_sync(1 + t, kBM);
+    if (ok && my_blocks > 0 && r == 0) {
+#pragma unroll
+      for (int p = 0; p < L::kPanels; ++p) tma_store_3d(&tm_o, sQ(t) + p * kPanelBytes, 64 * p, row0 + kBM * t, bh);
+      tma_store_commit();
+      tma_store_wait0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, int NQ, int STAGES, bool BF16>
+cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                         const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<D, NQ, STAGES>;
+  auto kern = fa_fwd_kernel<D, NQ, STAGES, BF16>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
+  if (err != cudaSuccess) return err;
+  const long long grid = (long long)a.num_qblocks * a.BH;
+  kern<<<(unsigned)grid, (4 * NQ + 2) * 32, L::kAlloc, stream>>>(q, k, v, o, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fwd_rows_per_cta(int d) { return d == 256 ? kBM : 2 * kBM; }
+
+cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream) {
+  switch (d) {
+    case 64:
+      return bf16 ? launch_fwd_t<64, 2, 4, true>(q, k, v, o, a, stream)
+                  : launch_fwd_t<64, 2, 4, false>(q, k, v, o, a, stream);
+    case 128:
+      return bf16 ? launch_fwd_t<128, 2, 3, true>(q, k, v, o, a, stream)
+                  : launch_fwd_t<128, 2, 3, false>(q, k, v, o, a, stream);
+    case 256:
+      return bf16 ? launch_fwd_t<256, 1, 2, true>(q, k, v, o, a, stream)
+                  : launch_fwd_t<256, 1, 2, false>(q, k, v, o, a, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

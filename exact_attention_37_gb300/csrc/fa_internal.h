@@ -1,0 +1,54 @@
+// Host-side declarations shared by the C-ABI layer and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Arguments of the forward kernel that are not TMA descriptors.
+struct FwdArgs {
+  float* lse;            // [B*H, N] fp32 logsumexp output
+  int N;                 // sequence length
+  int BH;                // batch * heads
+  int num_qblocks;       // ceil(N / rows per CTA)
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e): scores go to base 2 with one multiply
+  int causal;            // key j hidden from query i when j > i
+  uint32_t* err;         // device error word
+};
+
+// Arguments of the backward kernels that are not TMA descriptors.
+struct BwdArgs {
+  const void* o;         // [B*H, N, d] forward output (16-bit)
+  const void* dout;      // [B*H, N, d] upstream gradient (16-bit)
+  const float* lse;      // [B*H, N] logsumexp from the forward pass
+  float* dq_acc;         // [B*H, N, d] fp32 dQ accumulator (workspace)
+  float* delta;          // [B*H, N] fp32 D = rowsum(dO o O) (workspace)
+  void* dq;              // [B*H, N, d] 16-bit dQ output
+  void* dk;              // [B*H, N, d] 16-bit dK output
+  void* dv;              // [B*H, N, d] 16-bit dV output
+  int N;
+  int d;
+  int BH;
+  float scale;
+  float scale_log2;
+  int causal;
+  uint32_t* err;
+};
+
+// Rows of Q handled by one forward CTA for head dimension d.
+int fwd_rows_per_cta(int d);
+
+cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream);
+
+// Optional events recorded around the main backward kernel (measurement hook).
+extern cudaEvent_t g_bwd_main_before;
+extern cudaEvent_t g_bwd_main_after;
+
+cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,135 @@
+/*
+ * fa_attention.h -- C ABI of the exact-attention library for GB300 (sm_103a).
+ *
+ * What it computes
+ * ----------------
+ * Exact scaled-dot-product attention, O = softmax(Q K^T * scale + mask) V, the
+ * formula of the page "FlashAttention — فلاش أتنشن", section "The problem of
+ * standard attention" (there the scale is 1/sqrt(d_k)).  The forward pass is
+ * done the way the same page describes in its sections "Tiling and block
+ * processing", "Online softmax" and "Fusion of the operations into one CUDA
+ * kernel": Q, K, V tiles are staged on chip, each query row keeps a running
+ * maximum and a running sum of exponentials, masking is fused, and only the
+ * final output (plus one float per row) is written -- no N x N matrix ever
+ * reaches device memory.  The parallel split over (batch, head, query block) and
+ * over key blocks in the backward pass follows the page "FlashAttention-2 —
+ * فلاش أتنشن-2", section "Technical architecture", item 2 ("parallelism").
+ *
+ * Layout and types (every call)
+ * -----------------------------
+ *  - Q, K, V, O, dO, dQ, dK, dV: [B, H, N, d] contiguous, d innermost, element
+ *    type fp16 or bf16 (`fa_dtype`), all in the same type.
+ *  - lse (the per-row logsumexp L): [B, H, N] fp32, natural log of the sum of
+ *    exp(scaled, masked scores) of that row.
+ *  - d in {64, 128, 256}; N >= 0 (any value: ragged tails are masked); B, H >= 0;
+ *    B*H*N == 0 is an empty problem and returns FA_OK without launching work.
+ *  - causal != 0 hides key j from query i when j > i (square, top-left
+ *    aligned); masked scores are -inf before the softmax.
+ *  - Every pointer is a device pointer, 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory; the backward pass takes a caller-provided workspace whose size
+ * `fa_bwd_workspace_size` reports (linear in N).  TMA descriptors are encoded
+ * on the host for every call and passed by value to the kernels.
+ *
+ * Errors: argument errors are detected on the host, return at once and launch
+ * nothing.  A failed launch returns FA_ERR_CUDA.  All calls are asynchronous on
+ * `stream`; a kernel that gave up on a bounded device-side wait records it in a
+ * device error word, which `fa_check_device_status` reports (it synchronizes
+ * the stream).  No kernel traps.
+ */
+#ifndef FA_ATTENTION_H_
+#define FA_ATTENTION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, scale not finite and > 0, bad enum */
+  FA_ERR_UNSUPPORTED = 2,    /* head dim outside {64,128,256}, sizes over the limits, no sm_103a device */
+  FA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,      /* backward workspace missing or smaller than fa_bwd_workspace_size */
+  FA_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up on a bounded wait (see fa_check_device_status) */
+} fa_status;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* The stream type of the CUDA runtime, spelled without including its headers. */
+typedef struct CUstream_st* fa_stream_t;
+
+/*
+ * Forward pass: O and L from Q, K, V.
+ *   q, k, v : inputs [B,H,N,d] (read only)
+ *   o       : output [B,H,N,d], same type as the inputs
+ *   lse     : output [B,H,N] fp32, L_i = ln sum_j exp(scale * q_i.k_j) over visible j
+ *   scale   : softmax scale, finite and > 0, normally 1/sqrt(d)
+ * Computation per page "FlashAttention — فلاش أتنشن", sections "Online softmax"
+ * and "Fusion of the operations into one CUDA kernel".
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace `fa_bwd` needs: an fp32 dQ accumulator [B,H,N,d],
+ * the fp32 row vector D [B,H,N], and alignment padding.  Linear in N.
+ * Returns 0 for invalid or empty sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass: dQ, dK, dV of the loss sum(O o dO), recomputing S and P from
+ * Q, K and the forward pass's L (no N x N matrix is stored).  The pages state
+ * that the method serves training (page "FlashAttention-2 — فلاش أتنشن-2",
+ * section "Performance and efficiency"); the gradients are the chain-rule
+ * derivatives of the attention formula:
+ *   D_i = sum_c dO_ic O_ic,  P = exp(scale*S - L),  dV = P^T dO,
+ *   dS = P o (dO V^T - D),   dQ = scale dS K,       dK = scale dS^T Q.
+ *   q,k,v,o,dout : inputs [B,H,N,d] (o is the forward output)
+ *   lse          : input [B,H,N] fp32 from fa_fwd
+ *   dq,dk,dv     : outputs [B,H,N,d], same type as the inputs
+ *   workspace    : device buffer of at least fa_bwd_workspace_size(B,H,N,d)
+ *                  bytes, 256-byte aligned; contents need not be initialised
+ *                  and are overwritten.
+ * Launches, in order on `stream`: the D pre-pass (which also zeroes the dQ
+ * accumulator), the key-block-parallel main kernel, and the dQ conversion.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device error word of the
+ * current device.  FA_OK if no kernel gave up on a wait since the last check,
+ * FA_ERR_DEVICE_TIMEOUT otherwise, FA_ERR_CUDA if the synchronization failed.
+ */
+fa_status fa_check_device_status(fa_stream_t stream);
+
+/* Raw device error word of the last fa_check_device_status (0 = none). */
+uint32_t fa_last_device_error_bits(void);
+
+/*
+ * Measurement hook: when both events are non-null, every later fa_bwd records
+ * `before` on its stream just before the main backward kernel and `after` just
+ * after it, so a caller can time that kernel alone with cudaEventElapsedTime.
+ * The events are CUDA runtime events (cudaEvent_t) owned by the caller; pass
+ * nulls to stop.  Not thread-safe: one setting per process.
+ */
+void fa_bwd_set_main_kernel_events(void* before, void* after);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(fa_status s);
+
+/* Library version, (major << 16) | minor. */
+uint32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_ATTENTION_H_ */

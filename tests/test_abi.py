@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every symbol include/fa_attention.h declares, and rejects bad arguments
+before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_37_gb300 import _lib
+from exact_attention_37_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_attention.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    return sorted({n for n in names if n.startswith("fa_")})
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_status", "fa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.fa_status_string(code).decode() == name
+    assert lib.fa_version() >> 16 == 1
+
+
+def fwd(lib, **over):
+    a = dict(q=16, k=16, v=16, o=16, lse=16, B=1, H=1, N=8, d=64, scale=0.125, causal=0, dtype=1)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["o"]), vp(a["lse"]), a["B"], a["H"], a["N"], a["d"],
+                      a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d=96), 2), (dict(d=32), 2), (dict(d=512), 2),
+    (dict(N=-1), 1), (dict(B=-2), 1), (dict(H=-1), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(dtype=7), 1),
+    (dict(q=0), 1), (dict(lse=0), 1),
+    (dict(k=24), 3), (dict(o=8), 3),
+])
+def test_fwd_rejects_bad_arguments_on_the_host(lib, over, code):
+    assert fwd(lib, **over) == code
+
+
+def test_fwd_empty_problem_is_a_no_op(lib):
+    assert fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert fwd(lib, B=0) == 0
+
+
+def bwd(lib, ws_bytes=None, **over):
+    a = dict(p=256, ws=256, B=1, H=2, N=10, d=128, scale=0.1, causal=1, dtype=0)
+    a.update(over)
+    vp = ctypes.c_void_p
+    ws_bytes = lib.fa_bwd_workspace_size(a["B"], a["H"], a["N"], a["d"]) if ws_bytes is None else ws_bytes
+    ptrs = [vp(a.get(n, a["p"])) for n in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv")]
+    return lib.fa_bwd(*ptrs, vp(a["ws"]), ws_bytes, a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"],
+                      a["dtype"], None)
+
+
+def test_bwd_rejects_bad_arguments_on_the_host(lib):
+    assert bwd(lib, d=80) == 2
+    assert bwd(lib, dq=0) == 1
+    assert bwd(lib, dk=40) == 3
+    assert bwd(lib, ws=0) == 4
+    assert bwd(lib, ws_bytes=100) == 4
+    assert bwd(lib, ws=256 + 16) == 3  # workspace must be 256-byte aligned
+    assert bwd(lib, B=0) == 0
+
+
+def test_workspace_is_linear_in_n(lib):
+    sizes = [lib.fa_bwd_workspace_size(2, 16, n, 128) for n in (1024, 2048, 4096, 8192)]
+    per_row = (128 + 1) * 4
+    for n, s in zip((1024, 2048, 4096, 8192), sizes):
+        assert s >= 2 * 16 * n * per_row
+        assert s <= 2 * 16 * n * per_row + 512
+    assert lib.fa_bwd_workspace_size(1, 1, 0, 64) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 8, 96) == 0
+
+
+def test_valid_call_without_a_device_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert fwd(lib) in (2, 5)

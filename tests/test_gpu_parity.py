@@ -1,0 +1,121 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small problems are compared element by element over every head; they span
+several 128-row tiles and a ragged tail.  The five workloads of the method's
+evaluation are run at full size in the launch configuration the bench uses and
+checked on sampled heads and rows.  Tolerances are in tests/parity.py.
+"""
+import pytest
+import torch
+
+import exact_attention_37_gb300 as fa
+from exact_attention_37_gb300 import synth
+from exact_attention_37_gb300.synth import Workload
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from exact_attention_37_gb300 import build
+
+    build.build()
+    fa.load()
+
+
+def small(N, d, dtype, causal, B=1, H=2, scale=1.0, seeds=(101, 102, 103, 104)):
+    return Workload(f"small_N{N}_d{d}_{dtype}_{'c' if causal else 'nc'}", B, H, N, d, dtype, causal, scale, seeds)
+
+
+# --------------------------------------------------------------------- forward, exact over all elements
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_small(d, dtype, causal):
+    parity.check_forward_full(small(300, d, dtype, causal))
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_ragged_lengths(N, causal):
+    parity.check_forward_full(small(N, 128, "bf16", causal, B=1, H=1))
+
+
+def test_forward_tiny_workload():
+    parity.check_forward_full(synth.TINY)
+
+
+def test_forward_many_heads_few_rows():
+    parity.check_forward_full(small(64, 64, "fp16", True, B=3, H=5))
+
+
+def test_forward_empty():
+    q = torch.empty(1, 2, 0, 64, dtype=torch.float16, device="cuda")
+    o, lse = fa.forward(q, q, q)
+    assert o.shape == q.shape and lse.shape == (1, 2, 0)
+
+
+# --------------------------------------------------------------------- backward, exact over all elements
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_small(d, dtype, causal):
+    parity.check_backward_full(small(300, d, dtype, causal))
+
+
+@pytest.mark.parametrize("N", [1, 64, 65, 127, 129, 200])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_ragged_lengths(N, d):
+    parity.check_backward_full(small(N, d, "bf16", True, B=1, H=1))
+
+
+# --------------------------------------------------------------------- the five workloads at full size
+def test_train_workload_forward_sampled():
+    w = synth.TRAIN
+    for causal in (False, True):
+        wc = w.with_(causal=causal)
+        parity.check_forward_sampled(wc, synth.sample_heads(wc), synth.sample_rows(wc.N, 48))
+
+
+def test_train_workload_backward_sampled():
+    for causal in (False, True):
+        wc = synth.TRAIN.with_(causal=causal)
+        parity.check_backward_sampled(wc, synth.sample_heads(wc, count=3))
+
+
+def test_long_workload_forward_sampled():
+    w = synth.LONG
+    parity.check_forward_sampled(w, synth.sample_heads(w), synth.sample_rows(w.N, 64))
+
+
+def test_long_workload_backward_sampled():
+    w = synth.LONG
+    parity.check_backward_sampled(w, synth.sample_heads(w, count=2))
+
+
+def test_d256_workload_forward_sampled():
+    for causal in (False, True):
+        w = synth.D256.with_(causal=causal)
+        parity.check_forward_sampled(w, synth.sample_heads(w), synth.sample_rows(w.N, 48))
+
+
+def test_d256_workload_backward_sampled():
+    for causal in (False, True):
+        w = synth.D256.with_(causal=causal)
+        parity.check_backward_sampled(w, synth.sample_heads(w, count=2))
+
+
+def test_ctx32k_workload_forward_sampled_and_linear_memory():
+    w = synth.CTX32K
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    parity.check_forward_sampled(w, synth.sample_heads(w), synth.sample_rows(w.N, 64))
+    torch.cuda.synchronize()
+    # q, k, v, o (16-bit) and L are the only device buffers: no N x N matrix exists
+    # (one fp32 score matrix of this workload would take 137 GB).
+    peak = torch.cuda.max_memory_allocated()
+    n_elem = w.B * w.H * w.N * w.d
+    assert peak <= 4 * n_elem * 2 + w.B * w.H * w.N * 4 + (256 << 20)
