@@ -231,16 +231,19 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait(bar(L::kPdsFull), it & 1, args.err, kErrTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        // Scores of the next block first, so the softmax warps can start on them
-        // while the tensor cores compute this block's gradients.
-        if (it + 1 < nit) {
+        auto next_scores = [&]() -> bool {
           const int s1 = (it + 1) % STG;
-          ok = mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma);
-          if (!ok) break;
+          if (!mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma)) return false;
           tc_fence_after();
           issue_sdp(s1);
           mma_commit(bar(L::kSFull));
-        }
+          return true;
+        };
+        // With two or more Q/dO stages, the next block's scores go first so the
+        // softmax warps can start on them while the tensor cores compute this
+        // block's gradients.  With one stage the next tile can only arrive after
+        // this block's gradients have released the stage.
+        if (STG > 1 && it + 1 < nit && !(ok = next_scores())) break;
         if (it > 0) {
           ok = mbar_wait(bar(L::kDqFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax);
           if (!ok) break;
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(320, 1)
         issue_grads(s, it);
         mma_commit(bar(L::kGrads));
         mma_commit(bar(L::kQEmpty + s));
+        if (STG == 1 && it + 1 < nit && !(ok = next_scores())) break;
       }
       mma_commit(bar(L::kDrain));
       mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);

@@ -4,7 +4,10 @@ compare it with the fp64 oracle on the same rounded inputs.
 Tolerances (written here, used by every GPU test):
   O  : max|g - r| <= 2e-2 (bf16) / 5e-3 (fp16), and max|g - r| / max|r| <= 2e-2
   L  : max|g - r| <= 1e-3
-  dQ, dK, dV : max|g - r| / max|r| <= 5e-2
+  dQ, dK, dV : max|g - r| / max(max|r|, 1e-3) <= 5e-2
+The 1e-3 floor only matters when the reference gradient is (near) zero, e.g. N = 1
+where dS = P (dP - D) vanishes identically and what remains is the rounding of O
+to 16 bits inside D; it caps the absolute error there at 5e-5.
 """
 from __future__ import annotations
 
@@ -46,9 +49,12 @@ def compare_l(got, ref):
     return err
 
 
+G_FLOOR = 1e-3
+
+
 def compare_g(got, ref, what):
     err = float(np.abs(got - ref).max()) if got.size else 0.0
-    mref = float(np.abs(ref).max()) if ref.size else 1.0
+    mref = max(float(np.abs(ref).max()) if ref.size else 1.0, G_FLOOR)
     assert err <= G_REL * mref, f"{what}: max err {err:.3e} > {G_REL} * max|ref| {mref:.3e}"
     return err / max(mref, 1e-30)
 
