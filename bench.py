@@ -252,27 +252,28 @@ def main():
     fa.fa_check_device_status()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    fa.fa_profile_begin(2 * K)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         for i in range(K):
             flush.zero_()
-            e0, e1, e2, e3, e4 = ev[i]
-            fa.fa_bwd_set_main_kernel_events(e2, e3)
+            e0, e1, e2 = ev[i]
             e0.record(stream)
             fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
             e1.record(stream)
             fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
-            e4.record(stream)
+            e2.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    fa.fa_bwd_set_main_kernel_events(None, None)
+    kernels = fa.fa_profile_end()
     fa.fa_check_device_status()
-    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
-    bwd_main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    fwd_kernel_ms = [ms for kind, ms in kernels if kind == "fwd"]
+    bwd_main_ms = [ms for kind, ms in kernels if kind == "bwd"]
     total_ms = reduce_max(sum(step_ms), world, dev)
     ms_per_step = total_ms / K
 
@@ -307,7 +308,7 @@ def main():
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
-    fwd_avg = statistics.mean(fwd_ms)
+    fwd_avg = statistics.mean(fwd_kernel_ms)
     bwd_main_avg = statistics.mean(bwd_main_ms)
     flops_bwd = flops_step - flops_fwd
     if bwd_main_avg >= fwd_avg:

@@ -18,7 +18,8 @@ from ._lib import (  # noqa: F401
     FA_FP16,
     FaError,
     fa_bwd,
-    fa_bwd_set_main_kernel_events,
+    fa_profile_begin,
+    fa_profile_end,
     fa_bwd_workspace_size,
     fa_check_device_status,
     fa_fwd,

@@ -34,7 +34,8 @@ SIGNATURES = {
     "fa_check_device_status": (_i, [_vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
     "fa_status_string": (ctypes.c_char_p, [_i]),
-    "fa_bwd_set_main_kernel_events": (None, [_vp, _vp]),
+    "fa_profile_begin": (_i, [_i]),
+    "fa_profile_end": (_i, [_vp, _vp, _i]),
     "fa_version": (ctypes.c_uint32, []),
 }
 
@@ -133,11 +134,19 @@ def fa_check_device_status(stream=None):
     _check("fa_check_device_status", load().fa_check_device_status(_stream(stream)))
 
 
-def fa_bwd_set_main_kernel_events(before=None, after=None):
-    """Record torch.cuda.Event ``before``/``after`` around the main backward kernel (None, None to stop)."""
-    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
-    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
-    load().fa_bwd_set_main_kernel_events(b, a)
+def fa_profile_begin(n: int):
+    """Record the main-kernel time of the next ``n`` fa_fwd / fa_bwd calls."""
+    _check("fa_profile_begin", load().fa_profile_begin(int(n)))
+
+
+def fa_profile_end(max_out: int = 65536):
+    """Wait for the recorded events; returns [(kind, ms)] in call order, kind 'fwd' or 'bwd'."""
+    ms = (ctypes.c_float * max_out)()
+    kind = (ctypes.c_int * max_out)()
+    n = load().fa_profile_end(ms, kind, max_out)
+    if n < 0:
+        raise FaError("fa_profile_end", 5)
+    return [("fwd" if kind[i] == 0 else "bwd", float(ms[i])) for i in range(n)]
 
 
 def fa_status_string(code: int) -> str:

@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
@@ -100,7 +102,44 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Library-owned events for the measurement hook.
+struct Profile {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+  std::vector<int> kind;
+  int used = 0;
+  bool on = false;
+  bool open = false;  // a begin mark is waiting for its end mark
+  void release() {
+    for (auto& e : ev) {
+      if (e.first) cudaEventDestroy(e.first);
+      if (e.second) cudaEventDestroy(e.second);
+    }
+    ev.clear();
+    kind.clear();
+    used = 0;
+    on = false;
+    open = false;
+  }
+};
+Profile& profile() {
+  static Profile p;
+  return p;
+}
+
 }  // namespace
+
+void profile_mark_begin(cudaStream_t stream) {
+  Profile& p = profile();
+  if (!p.on || p.used >= (int)p.ev.size()) return;
+  if (cudaEventRecord(p.ev[p.used].first, stream) == cudaSuccess) p.open = true;
+}
+
+void profile_mark_end(cudaStream_t stream, int kind) {
+  Profile& p = profile();
+  if (!p.on || !p.open) return;
+  p.open = false;
+  if (cudaEventRecord(p.ev[p.used].second, stream) == cudaSuccess) p.kind[p.used++] = kind;
+}
 
 int bwd_query_rows(int d);
 
@@ -217,9 +256,41 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-void fa_bwd_set_main_kernel_events(void* before, void* after) {
-  g_bwd_main_before = static_cast<cudaEvent_t>(before);
-  g_bwd_main_after = static_cast<cudaEvent_t>(after);
+fa_status fa_profile_begin(int n) {
+  if (n < 0 || n > 65536) return FA_ERR_INVALID_ARG;
+  Profile& p = profile();
+  p.release();
+  p.ev.resize((size_t)n);
+  p.kind.assign((size_t)n, 0);
+  for (auto& e : p.ev) {
+    if (cudaEventCreate(&e.first) != cudaSuccess || cudaEventCreate(&e.second) != cudaSuccess) {
+      p.release();
+      return FA_ERR_CUDA;
+    }
+  }
+  p.used = 0;
+  p.open = false;
+  p.on = n > 0;
+  return FA_OK;
+}
+
+int fa_profile_end(float* out_ms, int* out_kind, int max_out) {
+  Profile& p = profile();
+  int written = 0;
+  bool failed = false;
+  for (int i = 0; i < p.used && i < max_out; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.ev[i].second) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, p.ev[i].first, p.ev[i].second) != cudaSuccess) {
+      failed = true;
+      break;
+    }
+    if (out_ms) out_ms[i] = ms;
+    if (out_kind) out_kind[i] = p.kind[i];
+    ++written;
+  }
+  p.release();
+  return failed ? -1 : written;
 }
 
 uint32_t fa_version(void) { return (1u << 16) | 0u; }

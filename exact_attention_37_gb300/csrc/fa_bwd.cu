@@ -494,11 +494,11 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
     if (e != cudaSuccess) return e;
     const long long nkb = (a.N + kBN - 1) / kBN;
     const long long grid = nkb * a.BH * (D / DH);
-    if (g_bwd_main_before && g_bwd_main_after) cudaEventRecord(g_bwd_main_before, stream);
+    profile_mark_begin(stream);
     kern<<<(unsigned)grid, 320, L::kAlloc, stream>>>(q, k, v, dout, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (g_bwd_main_before && g_bwd_main_after) cudaEventRecord(g_bwd_main_after, stream);
+    profile_mark_end(stream, 1);
   }
   // 3) dQ conversion
   {
@@ -510,9 +510,6 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
 }
 
 }  // namespace
-
-cudaEvent_t g_bwd_main_before = nullptr;
-cudaEvent_t g_bwd_main_after = nullptr;
 
 int bwd_query_rows(int d) { return d == 64 ? 128 : 64; }
 

@@ -395,8 +395,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
   if (err != cudaSuccess) return err;
   const long long grid = (long long)a.num_qblocks * a.BH;
+  profile_mark_begin(stream);
   kern<<<(unsigned)grid, (4 * NQ + 2) * 32, L::kAlloc, stream>>>(q, k, v, o, a);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  profile_mark_end(stream, 0);
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -44,9 +44,9 @@ int fwd_rows_per_cta(int d);
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream);
 
-// Optional events recorded around the main backward kernel (measurement hook).
-extern cudaEvent_t g_bwd_main_before;
-extern cudaEvent_t g_bwd_main_after;
+// Measurement hook: events around a main kernel while profiling is on (no-ops otherwise).
+void profile_mark_begin(cudaStream_t stream);
+void profile_mark_end(cudaStream_t stream, int kind);
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);

@@ -114,13 +114,19 @@ fa_status fa_check_device_status(fa_stream_t stream);
 uint32_t fa_last_device_error_bits(void);
 
 /*
- * Measurement hook: when both events are non-null, every later fa_bwd records
- * `before` on its stream just before the main backward kernel and `after` just
- * after it, so a caller can time that kernel alone with cudaEventElapsedTime.
- * The events are CUDA runtime events (cudaEvent_t) owned by the caller; pass
- * nulls to stop.  Not thread-safe: one setting per process.
+ * Measurement hook.  fa_profile_begin(n) makes the next n calls of fa_fwd and
+ * fa_bwd record a pair of CUDA events (created and owned by the library) on
+ * their stream around their main kernel -- the fused forward kernel, or the
+ * key-block backward kernel without its pre-pass and dQ conversion.
+ * fa_profile_end waits for those events, writes each kernel's time in
+ * milliseconds to out_ms[i] and its kind to out_kind[i] (0 forward, 1 backward),
+ * in call order, stops recording and returns the number of entries written (at
+ * most max_out), or -1 if the events could not be read.  Returns of
+ * fa_profile_begin: FA_OK, FA_ERR_INVALID_ARG (n < 0 or n > 65536), FA_ERR_CUDA
+ * (event creation failed).  Not thread-safe: one recording per process.
  */
-void fa_bwd_set_main_kernel_events(void* before, void* after);
+fa_status fa_profile_begin(int n);
+int fa_profile_end(float* out_ms, int* out_kind, int max_out);
 
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(fa_status s);
