@@ -265,16 +265,29 @@ __global__ void __launch_bounds__(320, 1)
     const float c = args.scale_log2;
     float* sL = reinterpret_cast<float*>(smem + L::kLD);  // [2][2][BM]: (L*log2e, D) per buffer
     const size_t row_base = (size_t)bh * N;
+    constexpr int kCh = BM / 32;  // 32-column chunks per block
+    // L and D of query row (block it, row r) are fetched one block ahead, so the
+    // global-memory latency overlaps the previous block's work.
+    float pf_l = 0.f, pf_d = 0.f;
+    bool pf_in = false;
+    auto prefetch = [&](int it) {
+      const int q = (i_begin + it) * BM + r;
+      pf_in = (r < BM) && (it < nit) && (q < N);
+      if (pf_in) {
+        pf_l = __ldg(args.lse + row_base + q);
+        pf_d = __ldg(args.delta + row_base + q);
+      }
+    };
+    prefetch(0);
     for (int it = 0; it < nit; ++it) {
-      const int i = i_begin + it;
-      const int q0 = i * BM;
+      const int q0 = (i_begin + it) * BM;
       float* bufL = sL + (it & 1) * 2 * BM;
       float* bufD = bufL + BM;
       if (r < BM) {
-        const int q = q0 + r;
-        bufL[r] = (q < N) ? args.lse[row_base + q] * kLog2e : INFINITY;  // rows past N get P = 0
-        bufD[r] = (q < N) ? args.delta[row_base + q] : 0.f;
+        bufL[r] = pf_in ? pf_l * kLog2e : INFINITY;  // rows past N get P = 0
+        bufD[r] = pf_in ? pf_d : 0.f;
       }
+      prefetch(it + 1);
       named_bar_sync(1, 128);
       if (!mbar_wait(bar(L::kSFull), it & 1, args.err, kErrTimeoutMma)) break;
       tc_fence_after();
@@ -289,22 +302,36 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (!ok) break;
+      // TMEM reads are double-buffered: chunk ch+1 is in flight while chunk ch is computed.
+      uint32_t sv[2][32], dv[2][32];
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kColS, sv[0]);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP, dv[0]);
+      tmem_wait_ld();
+      reg_fence32(sv[0]);
+      reg_fence32(dv[0]);
 #pragma unroll
-      for (int ch = 0; ch < BM / 32; ++ch) {
-        uint32_t sv[32], dv[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + 32 * ch, sv);
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + 32 * ch, dv);
-        tmem_wait_ld();
-        reg_fence32(sv);
-        reg_fence32(dv);
+      for (int ch = 0; ch < kCh; ++ch) {
+        const int b = ch & 1;
+        if (ch + 1 < kCh) {
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + 32 * (ch + 1), sv[b ^ 1]);
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + 32 * (ch + 1), dv[b ^ 1]);
+        }
         float p[32], ds[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = 32 * ch + e;
-          float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -bufL[col]));
-          if (diag && key > q0 + col) pe = 0.f;
-          p[e] = pe;
-          ds[e] = pe * (__uint_as_float(dv[e]) - bufD[col]);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int col = 32 * ch + 4 * e4;
+          const float4 l4 = *reinterpret_cast<const float4*>(bufL + col);
+          const float4 d4 = *reinterpret_cast<const float4*>(bufD + col);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = 4 * e4 + u;
+            float pe = ex2_approx(fmaf(__uint_as_float(sv[b][e]), c, -lv[u]));
+            if (diag && key > q0 + col + u) pe = 0.f;
+            p[e] = pe;
+            ds[e] = pe * (__uint_as_float(dv[b][e]) - dd[u]);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -321,6 +348,11 @@ __global__ void __launch_bounds__(320, 1)
             st_shared_v4(sPt + off, pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
             st_shared_v4(sDSt + off, dw[w], dw[w + 1], dw[w + 2], dw[w + 3]);
           }
+        }
+        if (ch + 1 < kCh) {
+          tmem_wait_ld();
+          reg_fence32(sv[b ^ 1]);
+          reg_fence32(dv[b ^ 1]);
         }
       }
       tc_fence_before();  // done reading S^T and dP^T from TMEM
