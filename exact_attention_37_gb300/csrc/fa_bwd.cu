@@ -27,9 +27,12 @@
 // 128-row query blocks, or dQ_i^T = K_j^T dS^T for 64-row query blocks so that
 // the accumulator keeps M = 128.
 //
-// Warp roles: warps 0-3 turn S^T and dP^T into P^T and dS^T; warps 4-7 drain
-// dQ from TMEM into the fp32 accumulator and write dK, dV at the end; warp 8
-// issues TMA loads; warp 9 issues the tcgen05 MMAs.
+// Warp roles: warps 0-7 (two warpgroups, half of the query columns each) turn
+// S^T and dP^T into P^T and dS^T, releasing the S^T/dP^T accumulators as soon
+// as they have read them so the next block's scores overlap this block's
+// exponentials; warps 8-11 drain dQ from TMEM into the fp32 accumulator and
+// write dK, dV at the end; warp 12 issues TMA loads; warp 13 issues the tcgen05
+// MMAs.
 #include <algorithm>
 
 #include "fa_internal.h"
@@ -39,11 +42,17 @@ namespace fa {
 namespace {
 
 constexpr int kBN = 128;   // keys per CTA (= TMEM lanes)
+// Warp roles: 0-7 elementwise (two warpgroups), 8-11 dQ drain and epilogue, 12 TMA, 13 MMA.
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr int kBwdThreads = 14 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // D, DH: head dim and gradient columns per CTA; BM: query rows per block;
-// DQT: compute dQ^T (M = DH) instead of dQ (M = BM); STG: Q/dO pipeline depth.
-template <int D, int DH, int BM, bool DQT, int STG>
+// DQT: compute dQ^T (M = DH) instead of dQ (M = BM); STG: Q/dO pipeline depth;
+// NPB: P^T/dS^T tile buffers (2 lets the softmax warps write block i+1 while the
+// tensor cores still read block i).
+template <int D, int DH, int BM, bool DQT, int STG, int NPB>
 struct BwdLayout {
   static constexpr uint32_t kKVPanel = kBN * 128;                 // 128 key rows x 128 B
   static constexpr uint32_t kQPanel = BM * 128;                   // BM query rows x 128 B
@@ -54,17 +63,19 @@ struct BwdLayout {
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kKVTile;
   static constexpr uint32_t kQ = kV + kKVTile;                    // STG stages of (Q, dO)
-  static constexpr uint32_t kPt = kQ + STG * 2 * kQTile;
-  static constexpr uint32_t kDSt = kPt + kPdsTile;
-  static constexpr uint32_t kLD = kDSt + kPdsTile;                // 2 buffers x (L, D) x BM floats
+  static constexpr uint32_t kPds = kQ + STG * 2 * kQTile;         // NPB x (P^T, dS^T)
+  static constexpr uint32_t pt(int b) { return kPds + 2u * kPdsTile * b; }
+  static constexpr uint32_t dst(int b) { return kPds + 2u * kPdsTile * b + kPdsTile; }
+  static constexpr uint32_t kLD = kPds + 2u * kPdsTile * NPB;     // 2 buffers x (L, D) x BM floats
   static constexpr uint32_t kBar = kLD + 2 * 2 * BM * 4;
   static constexpr int kKVFull = 0;
   static constexpr int kQFull = 1;
   static constexpr int kQEmpty = kQFull + STG;
   static constexpr int kSFull = kQEmpty + STG;
-  static constexpr int kPdsFull = kSFull + 1;
-  static constexpr int kGrads = kPdsFull + 1;
-  static constexpr int kDqFree = kGrads + 1;
+  static constexpr int kSdpFree = kSFull + 1;
+  static constexpr int kPdsFull = kSdpFree + 1;                   // two, used alternately
+  static constexpr int kGrads = kPdsFull + 2;                     // one per P^T/dS^T buffer
+  static constexpr int kDqFree = kGrads + NPB;
   static constexpr int kDrain = kDqFree + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
@@ -95,26 +106,31 @@ __device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b,
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdArgs args) {
-  using L = BwdLayout<D, DH, BM, DQT, STG>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
   constexpr int kHalves = D / DH;
+  constexpr int kCW = BM / 2;        // query columns per elementwise warpgroup
+  constexpr int kNCh = kCW / 32;     // 32-column TMEM chunks per elementwise thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   auto sQ = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s; };
   auto sDO = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s + L::kQTile; };
-  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sPt = sbase + L::kPt, sDSt = sbase + L::kDSt;
+  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
+  auto sPt = [&](int b) -> uint32_t { return sbase + L::pt(b); };
+  auto sDSt = [&](int b) -> uint32_t { return sbase + L::dst(b); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = args.N;
 
-  // Work tile: key block kb (lowest first: under the causal mask it has the most query blocks).
+  // Work tile: the lowest key blocks first across all heads (under the causal mask
+  // they have the most query blocks), so the last wave holds the lightest work.
   const int tiles_per_kb = args.BH * kHalves;
   const int kb = (int)(blockIdx.x / tiles_per_kb);
   const int rem = (int)(blockIdx.x % tiles_per_kb);
@@ -132,17 +148,19 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(L::kQEmpty + s), 1);
     }
     mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kPdsFull), 128);
-    mbar_init(bar(L::kGrads), 1);
+    mbar_init(bar(L::kSdpFree), 256);
+    mbar_init(bar(L::kPdsFull + 0), 256);
+    mbar_init(bar(L::kPdsFull + 1), 256);
+    for (int b = 0; b < NPB; ++b) mbar_init(bar(L::kGrads + b), 1);
     mbar_init(bar(L::kDqFree), 128);
     mbar_init(bar(L::kDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(sbase + L::kTmemSlot, L::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -153,7 +171,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-  if (warp == 8) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(bar(L::kKVFull), 2 * L::kKVTile);
@@ -174,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_f16(BF16, kBN, BM, false, false);     // S^T, dP^T: M=128 keys, N=BM
@@ -189,21 +207,31 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t b_off = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
           mma_ss(tmem + L::kColS, make_sdesc_sw128(sK + a_off, 16, 1024), make_sdesc_sw128(sQ(s) + b_off, 16, 1024),
                  kIdS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kKVPanel + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
           mma_ss(tmem + L::kColDP, make_sdesc_sw128(sV + a_off, 16, 1024),
                  make_sdesc_sw128(sDO(s) + b_off, 16, 1024), kIdS, kk > 0);
         }
       };
       auto issue_grads = [&](int s, int it) {
+        const int pb = it % NPB;
         // dV += P^T dO, dK += dS^T Q: A K-major over the BM queries, B MN-major (DH columns).
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk) {
           const uint32_t a_off = (kk >> 2) * L::kPdsPanel + (kk & 3) * 32;
           const uint32_t b_off = hp * L::kQPanel + kk * 2048;
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ss(tmem + L::kColDV, make_sdesc_sw128(sPt + a_off, 16, 1024),
-                 make_sdesc_sw128(sDO(s) + b_off, L::kQPanel, 1024), kIdG, acc);
-          mma_ss(tmem + L::kColDK, make_sdesc_sw128(sDSt + a_off, 16, 1024),
-                 make_sdesc_sw128(sQ(s) + b_off, L::kQPanel, 1024), kIdG, acc);
+          mma_ss(tmem + L::kColDV, make_sdesc_sw128(sPt(pb) + a_off, 16, 1024),
+                 make_sdesc_sw128(sDO(s) + b_off, L::kQPanel, 1024), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kPdsPanel + (kk & 3) * 32;
+          const uint32_t b_off = hp * L::kQPanel + kk * 2048;
+          mma_ss(tmem + L::kColDK, make_sdesc_sw128(sDSt(pb) + a_off, 16, 1024),
+                 make_sdesc_sw128(sQ(s) + b_off, L::kQPanel, 1024), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
         }
         // dQ (or dQ^T) over the 128 keys of this block; both operands MN-major.
 #pragma unroll
@@ -212,12 +240,20 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t ds_off = kk * 2048;
           if constexpr (DQT) {
             mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024),
-                   make_sdesc_sw128(sDSt + ds_off, L::kPdsPanel, 1024), kIdQ, kk > 0);
+                   make_sdesc_sw128(sDSt(pb) + ds_off, L::kPdsPanel, 1024), kIdQ, kk > 0);
           } else {
-            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sDSt + ds_off, L::kPdsPanel, 1024),
+            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sDSt(pb) + ds_off, L::kPdsPanel, 1024),
                    make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024), kIdQ, kk > 0);
           }
         }
+      };
+      auto next_scores = [&](int it) -> bool {
+        const int s1 = (it + 1) % STG;
+        if (!mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma)) return false;
+        tc_fence_after();
+        issue_sdp(s1);
+        mma_commit(bar(L::kSFull));
+        return true;
       };
       bool ok = mbar_wait(bar(L::kKVFull), 0, args.err, kErrTimeoutTma);
       if (ok) ok = mbar_wait(bar(L::kQFull + 0), 0, args.err, kErrTimeoutTma);
@@ -228,51 +264,49 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int it = 0; ok && it < nit; ++it) {
         const int s = it % STG;
-        ok = mbar_wait(bar(L::kPdsFull), it & 1, args.err, kErrTimeoutSoftmax);
+        // Scores of the next block as soon as this block's S^T/dP^T have been read
+        // out of TMEM, so they run while the elementwise warps exponentiate.
+        // (With one Q/dO stage the next tile only arrives after this block's
+        // gradients release the stage, so they go after the gradients.)
+        if (STG > 1 && it + 1 < nit) {
+          ok = mbar_wait(bar(L::kSdpFree), it & 1, args.err, kErrTimeoutSoftmax);
+          if (!ok || !(ok = next_scores(it))) break;
+        }
+        ok = mbar_wait(bar(L::kPdsFull + (it & 1)), (it >> 1) & 1, args.err, kErrTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        auto next_scores = [&]() -> bool {
-          const int s1 = (it + 1) % STG;
-          if (!mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma)) return false;
-          tc_fence_after();
-          issue_sdp(s1);
-          mma_commit(bar(L::kSFull));
-          return true;
-        };
-        // With two or more Q/dO stages, the next block's scores go first so the
-        // softmax warps can start on them while the tensor cores compute this
-        // block's gradients.  With one stage the next tile can only arrive after
-        // this block's gradients have released the stage.
-        if (STG > 1 && it + 1 < nit && !(ok = next_scores())) break;
         if (it > 0) {
           ok = mbar_wait(bar(L::kDqFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax);
           if (!ok) break;
           tc_fence_after();
         }
         issue_grads(s, it);
-        mma_commit(bar(L::kGrads));
+        mma_commit(bar(L::kGrads + it % NPB));
         mma_commit(bar(L::kQEmpty + s));
-        if (STG == 1 && it + 1 < nit && !(ok = next_scores())) break;
+        if (STG == 1 && it + 1 < nit && !(ok = next_scores(it))) break;
       }
       mma_commit(bar(L::kDrain));
       mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P^T and dS^T
-    const int r = (warp << 5) + lane;  // key row inside the block == TMEM lane
+    // Two warpgroups; warpgroup e handles query columns [e*kCW, (e+1)*kCW) of the block.
+    const int e = warp >> 2;
+    const int wq = warp & 3;
+    const int r = (wq << 5) + lane;  // key row inside the block == TMEM lane
     const int key = key0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int cbeg = e * kCW;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float c = args.scale_log2;
     float* sL = reinterpret_cast<float*>(smem + L::kLD);  // [2][2][BM]: (L*log2e, D) per buffer
     const size_t row_base = (size_t)bh * N;
-    constexpr int kCh = BM / 32;  // 32-column chunks per block
-    // L and D of query row (block it, row r) are fetched one block ahead, so the
-    // global-memory latency overlaps the previous block's work.
+    // L and D of query column (block it, column cbeg + r) are fetched one block
+    // ahead, so the global-memory latency overlaps the previous block's work.
     float pf_l = 0.f, pf_d = 0.f;
     bool pf_in = false;
     auto prefetch = [&](int it) {
-      const int q = (i_begin + it) * BM + r;
-      pf_in = (r < BM) && (it < nit) && (q < N);
+      const int q = (i_begin + it) * BM + cbeg + r;
+      pf_in = (r < kCW) && (it < nit) && (q < N);
       if (pf_in) {
         pf_l = __ldg(args.lse + row_base + q);
         pf_d = __ldg(args.delta + row_base + q);
@@ -283,104 +317,95 @@ __global__ void __launch_bounds__(320, 1)
       const int q0 = (i_begin + it) * BM;
       float* bufL = sL + (it & 1) * 2 * BM;
       float* bufD = bufL + BM;
-      if (r < BM) {
-        bufL[r] = pf_in ? pf_l * kLog2e : INFINITY;  // rows past N get P = 0
-        bufD[r] = pf_in ? pf_d : 0.f;
+      if (r < kCW) {
+        bufL[cbeg + r] = pf_in ? pf_l * kLog2e : INFINITY;  // rows past N get P = 0
+        bufD[cbeg + r] = pf_in ? pf_d : 0.f;
       }
       prefetch(it + 1);
-      named_bar_sync(1, 128);
+      named_bar_sync(1 + e, 128);
       if (!mbar_wait(bar(L::kSFull), it & 1, args.err, kErrTimeoutMma)) break;
       tc_fence_after();
       const bool diag = args.causal && (key0 + kBN - 1 > q0);  // some key of the block is after some query
-      uint32_t pw[BM / 2], dw[BM / 2];
+      const int pb = it % NPB;
+      // The P^T/dS^T buffer pb is free once the gradients of block it-NPB (its last reader) are done.
+      auto wait_buffer = [&]() -> bool {
+        if (it < NPB) return true;
+        if (!mbar_wait(bar(L::kGrads + pb), ((it / NPB) - 1) & 1, args.err, kErrTimeoutMma)) return false;
+        tc_fence_after();
+        return true;
+      };
+      uint32_t pw[kCW / 2], dw[kCW / 2];
       bool ok = true;
-      if constexpr (BM == 128) {
-        // Wide blocks: free the P^T / dS^T tiles first, then write chunk by chunk.
-        if (it > 0) {
-          ok = mbar_wait(bar(L::kGrads), (it - 1) & 1, args.err, kErrTimeoutMma);
-          tc_fence_after();
-        }
-      }
+      if constexpr (kNCh > 1) ok = wait_buffer();  // wide blocks write chunk by chunk
       if (!ok) break;
-      // TMEM reads are double-buffered: chunk ch+1 is in flight while chunk ch is computed.
-      uint32_t sv[2][32], dv[2][32];
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kColS, sv[0]);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP, dv[0]);
-      tmem_wait_ld();
-      reg_fence32(sv[0]);
-      reg_fence32(dv[0]);
 #pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) {
-        const int b = ch & 1;
-        if (ch + 1 < kCh) {
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + 32 * (ch + 1), sv[b ^ 1]);
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + 32 * (ch + 1), dv[b ^ 1]);
+      for (int ch = 0; ch < kNCh; ++ch) {
+        uint32_t sv[32], dv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + cbeg + 32 * ch, sv);
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + cbeg + 32 * ch, dv);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(dv);
+        if (ch == kNCh - 1) {
+          tc_fence_before();  // this thread is done reading S^T and dP^T from TMEM
+          mbar_arrive(bar(L::kSdpFree));
         }
         float p[32], ds[32];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const int col = 32 * ch + 4 * e4;
+          const int col = cbeg + 32 * ch + 4 * e4;
           const float4 l4 = *reinterpret_cast<const float4*>(bufL + col);
           const float4 d4 = *reinterpret_cast<const float4*>(bufD + col);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int e = 4 * e4 + u;
-            float pe = ex2_approx(fmaf(__uint_as_float(sv[b][e]), c, -lv[u]));
+            const int x = 4 * e4 + u;
+            float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lv[u]));
             if (diag && key > q0 + col + u) pe = 0.f;
-            p[e] = pe;
-            ds[e] = pe * (__uint_as_float(dv[b][e]) - dd[u]);
+            p[x] = pe;
+            ds[x] = pe * (__uint_as_float(dv[x]) - dd[u]);
           }
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pw[(ch * 32) / 2 + e] = pack2<BF16>(p[2 * e], p[2 * e + 1]);
-          dw[(ch * 32) / 2 + e] = pack2<BF16>(ds[2 * e], ds[2 * e + 1]);
+        for (int x = 0; x < 16; ++x) {
+          pw[16 * ch + x] = pack2<BF16>(p[2 * x], p[2 * x + 1]);
+          dw[16 * ch + x] = pack2<BF16>(ds[2 * x], ds[2 * x + 1]);
         }
-        if constexpr (BM == 128) {
-          // chunk ch covers 16-byte chunks 4ch..4ch+3 of the row
+        if constexpr (kNCh > 1) {
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const int chunk = ch * 4 + k4;
+            const int chunk = (cbeg + 32 * ch) / 8 + k4;  // 16-byte chunk index along the row
             const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
-            const int w = (ch * 32) / 2 + 4 * k4;
-            st_shared_v4(sPt + off, pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
-            st_shared_v4(sDSt + off, dw[w], dw[w + 1], dw[w + 2], dw[w + 3]);
+            const int w = 16 * ch + 4 * k4;
+            st_shared_v4(sPt(pb) + off, pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
+            st_shared_v4(sDSt(pb) + off, dw[w], dw[w + 1], dw[w + 2], dw[w + 3]);
           }
         }
-        if (ch + 1 < kCh) {
-          tmem_wait_ld();
-          reg_fence32(sv[b ^ 1]);
-          reg_fence32(dv[b ^ 1]);
-        }
       }
-      tc_fence_before();  // done reading S^T and dP^T from TMEM
-      if constexpr (BM != 128) {
-        if (it > 0) {
-          if (!mbar_wait(bar(L::kGrads), (it - 1) & 1, args.err, kErrTimeoutMma)) break;
-          tc_fence_after();
-        }
+      if constexpr (kNCh == 1) {
+        if (!wait_buffer()) break;
 #pragma unroll
-        for (int chunk = 0; chunk < BM / 8; ++chunk) {
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int chunk = cbeg / 8 + k4;
           const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
-          st_shared_v4(sPt + off, pw[4 * chunk], pw[4 * chunk + 1], pw[4 * chunk + 2], pw[4 * chunk + 3]);
-          st_shared_v4(sDSt + off, dw[4 * chunk], dw[4 * chunk + 1], dw[4 * chunk + 2], dw[4 * chunk + 3]);
+          st_shared_v4(sPt(pb) + off, pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
+          st_shared_v4(sDSt(pb) + off, dw[4 * k4], dw[4 * k4 + 1], dw[4 * k4 + 2], dw[4 * k4 + 3]);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(L::kPdsFull));
+      mbar_arrive(bar(L::kPdsFull + (it & 1)));
     }
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-    const int wq = warp - 4;
+    const int wq = warp - 8;
     const int r = (wq << 5) + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     float* dq_acc = args.dq_acc + (size_t)bh * N * D;
     bool ok = true;
     for (int it = 0; it < nit; ++it) {
       const int q0 = (i_begin + it) * BM;
-      ok = mbar_wait(bar(L::kGrads), it & 1, args.err, kErrTimeoutMma);
+      ok = mbar_wait(bar(L::kGrads + it % NPB), (it / NPB) & 1, args.err, kErrTimeoutMma);
       if (!ok) break;
       tc_fence_after();
       constexpr int kCh = L::kDqCols / 32;
@@ -398,9 +423,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int ch = 0; ch < kCh; ++ch)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int q = q0 + 32 * ch + e;
-            if (q < N) red_add(dq_acc + (size_t)q * D + col, __uint_as_float(v[ch][e]));
+          for (int x = 0; x < 32; ++x) {
+            const int q = q0 + 32 * ch + x;
+            if (q < N) red_add(dq_acc + (size_t)q * D + col, __uint_as_float(v[ch][x]));
           }
       } else {
         // lane r holds dQ row q0 + r, columns half*DH .. half*DH+DH-1
@@ -410,9 +435,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int ch = 0; ch < kCh; ++ch)
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + 32 * ch + e, __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]),
-                         __uint_as_float(v[ch][e + 2]), __uint_as_float(v[ch][e + 3]));
+            for (int x = 0; x < 32; x += 4)
+              red_add_v4(dst + 32 * ch + x, __uint_as_float(v[ch][x]), __uint_as_float(v[ch][x + 1]),
+                         __uint_as_float(v[ch][x + 2]), __uint_as_float(v[ch][x + 3]));
         }
       }
     }
@@ -433,12 +458,12 @@ __global__ void __launch_bounds__(320, 1)
           reg_fence32(v);
           if (key < N) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              st_global_v4(dst + 32 * ch + e,
-                           pack2<BF16>(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul),
-                           pack2<BF16>(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul),
-                           pack2<BF16>(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul),
-                           pack2<BF16>(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul));
+            for (int x = 0; x < 32; x += 8)
+              st_global_v4(dst + 32 * ch + x,
+                           pack2<BF16>(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
+                           pack2<BF16>(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
+                           pack2<BF16>(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
+                           pack2<BF16>(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
           }
         }
       }
@@ -447,7 +472,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -503,10 +528,10 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const BwdArgs ar
   }
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, bool BF16>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
 cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                          const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BM, DQT, STG>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -521,13 +546,13 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   }
   // 2) main kernel
   {
-    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, BF16>;
+    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
     if (e != cudaSuccess) return e;
     const long long nkb = (a.N + kBN - 1) / kBN;
     const long long grid = nkb * a.BH * (D / DH);
     profile_mark_begin(stream);
-    kern<<<(unsigned)grid, 320, L::kAlloc, stream>>>(q, k, v, dout, a);
+    kern<<<(unsigned)grid, kBwdThreads, L::kAlloc, stream>>>(q, k, v, dout, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark_end(stream, 1);
@@ -549,14 +574,14 @@ cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
     case 64:
-      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<64, 64, 128, false, 3, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, 1, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<64, 64, 128, false, 3, 1, false>(q, k, v, dout, a, stream);
     case 128:
-      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<128, 128, 64, true, 3, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, 2, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<128, 128, 64, true, 3, 2, false>(q, k, v, dout, a, stream);
     case 256:
-      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<256, 128, 64, true, 1, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, 1, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<256, 128, 64, true, 1, 1, false>(q, k, v, dout, a, stream);
     default:
       return cudaErrorInvalidValue;
   }

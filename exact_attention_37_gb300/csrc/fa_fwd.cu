@@ -12,23 +12,26 @@
 // فلاش أتنشن-2", section "Technical architecture", item 2).
 //
 // GB300 mapping (one CTA per 128*NQ query rows):
-//   warp 4*NQ     TMA producer: Q sub-tiles once, then K_j / V_j tiles through a
-//                 ring of STAGES shared-memory slots, in the order the MMA warp
-//                 consumes them (K_0, K_1, V_0, K_2, V_1, ...).
+//   warp 4*NQ     TMA producer: Q sub-tiles once, then K_0, V_0, K_1, V_1, ...
+//                 through a ring of STAGES shared-memory slots.
 //   warp 4*NQ+1   MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
-//                 O_t += P_t V_j into TMEM, with tcgen05.mma (fp32 accumulate).
-//                 S for block j+1 is issued before P V for block j, so the tensor
-//                 cores work while the softmax warps exponentiate.
+//                 O_t += P_t V_j with P_t read straight from TMEM (tcgen05.mma
+//                 with the A operand in tensor memory), so P never touches
+//                 shared memory.  Per block the order is P_0 V_j, S_0(j+1),
+//                 P_1 V_j, S_1(j+1): the tensor pipe runs in order, so S_t(j+1)
+//                 overwrites the TMEM columns of P_t only after P_t V_j has read
+//                 them, and while softmax warpgroup t works on one block the
+//                 tensor cores work on the other sub-tile.
 //   warps 4t..4t+3  softmax for query sub-tile t: thread r owns query row r and
 //                 TMEM lane r, so every row reduction stays inside one thread.
 //                 Scores are taken to base 2 with one FMA (scale*log2 e folded in),
-//                 exponentiated with ex2, summed, rounded to 16 bits and written to
-//                 shared memory as the A operand of the P V product.  The row's
-//                 reference maximum only moves when the new maximum exceeds it by
-//                 more than 8 (base 2); otherwise the old one is kept, which leaves
-//                 the result exact (all terms share one reference) and skips the
-//                 rescale of O.  When it moves, the thread rescales its O row in
-//                 TMEM before releasing P.
+//                 exponentiated with ex2, summed, rounded to 16 bits and stored
+//                 back into the first half of the row's S columns as P.  The
+//                 row's reference maximum only moves when the new maximum exceeds
+//                 it by more than 8 (base 2); otherwise the old one is kept, which
+//                 leaves the result exact (all terms share one reference) and
+//                 skips the rescale of O.  When it moves, the thread rescales its
+//                 O row in TMEM before releasing P.
 //   epilogue      O / l rounded to 16 bits, staged in the dead Q tile, stored by TMA;
 //                 L = m*scale + ln(l) written per row.
 #include "fa_internal.h"
@@ -47,22 +50,20 @@ struct FwdLayout {
   static constexpr uint32_t kTileBytes = kPanels * kPanelBytes;  // 128 rows x D 16-bit values
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kRing = kQ + NQ * kTileBytes;
-  static constexpr uint32_t kP = kRing + STAGES * kTileBytes;
-  static constexpr uint32_t kBar = kP + NQ * 2 * kPanelBytes;
+  static constexpr uint32_t kBar = kRing + STAGES * kTileBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kFull = 1;
   static constexpr int kEmpty = kFull + STAGES;
   static constexpr int kSFull = kEmpty + STAGES;
-  static constexpr int kSFree = kSFull + NQ;
-  static constexpr int kPFull = kSFree + NQ;
+  static constexpr int kPFull = kSFull + NQ;
   static constexpr int kODone = kPFull + NQ;
   static constexpr int kDrain = kODone + NQ;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024 B
-  // TMEM columns: S_t at 128*t, O_t after all S tiles.
+  // TMEM columns: S_t (P_t in its first 64 columns) at 128*t, O_t after all S tiles.
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t s_col(int t) { return 128u * t; }
   static constexpr uint32_t o_col(int t) { return 128u * NQ + (uint32_t)D * t; }
@@ -85,13 +86,13 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   auto sQ = [&](int t) -> uint32_t { return sbase + L::kQ + L::kTileBytes * t; };
   auto sRing = [&](int s) -> uint32_t { return sbase + L::kRing + L::kTileBytes * s; };
-  auto sP = [&](int t) -> uint32_t { return sbase + L::kP + 2u * kPanelBytes * t; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = args.N;
 
-  // Heaviest query blocks first: under the causal mask the last blocks see the most keys.
+  // Heaviest query blocks first across all heads (under the causal mask the last
+  // blocks see the most keys), so the last wave holds the lightest work.
   const int qb = args.num_qblocks - 1 - (int)(blockIdx.x / args.BH);
   const int bh = (int)(blockIdx.x % args.BH);
   const int row0 = qb * (kBM * NQ);
@@ -119,7 +120,6 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     }
     for (int t = 0; t < NQ; ++t) {
       mbar_init(bar(L::kSFull + t), 1);
-      mbar_init(bar(L::kSFree + t), kBM);
       mbar_init(bar(L::kPFull + t), kBM);
       mbar_init(bar(L::kODone + t), 1);
     }
@@ -150,21 +150,15 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_3d(sQ(t) + p * kPanelBytes, &tm_q, bar(L::kQFull), 64 * p, row0 + kBM * t, bh);
-      int e = 0;
-      auto load = [&](const CUtensorMap* m, int j) -> bool {
+      // K_0, V_0, K_1, V_1, ...: the order the MMA warp consumes them.
+      for (int e = 0; e < 2 * nb; ++e) {
         const int s = e % STAGES, u = e / STAGES;
-        if (u > 0 && !mbar_wait(bar(L::kEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) return false;
+        if (u > 0 && !mbar_wait(bar(L::kEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(L::kFull + s), L::kTileBytes);
+        const CUtensorMap* m = (e & 1) ? &tm_v : &tm_k;
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * j, bh);
-        ++e;
-        return true;
-      };
-      bool ok = load(&tm_k, 0);
-      for (int j = 0; ok && j < nb; ++j) {
-        if (j + 1 < nb) ok = load(&tm_k, j + 1);
-        if (ok) ok = load(&tm_v, j);
+          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * (e >> 1), bh);
       }
     }
   } else if (warp == kWarpMma) {
@@ -182,64 +176,47 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       };
       auto issue_pv = [&](int t, int s, int j) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + L::o_col(t), make_sdesc_sw128(sP(t) + a_off, 16, 1024),
+        for (int kk = 0; kk < kBN / 16; ++kk)  // P_t: 8 TMEM columns (16 keys) per step
+          mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + 8 * kk,
                  make_sdesc_sw128(sRing(s) + kk * 2048, kPanelBytes, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
       };
-      bool ok = mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
-      int e = 0;
+      auto wait_full = [&](int e) -> bool {
+        return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
+      };
+      bool ok = mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
       if (ok) {
-        const int s = e % STAGES;
-        ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
-        if (ok) {
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < NQ; ++t)
-            if (nblk[t] > 0) {
-              issue_s(t, s);
-              mma_commit(bar(L::kSFull + t));
-            }
-          mma_commit(bar(L::kEmpty + s));
-          ++e;
-        }
-      }
-      for (int j = 0; ok && j < nb; ++j) {
-        if (j + 1 < nb) {
-          const int s = e % STAGES;
-          ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < NQ; ++t)
-            if (ok && j + 1 < nblk[t]) {
-              ok = mbar_wait(bar(L::kSFree + t), j & 1, args.err, kErrTimeoutSoftmax);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(t, s);
-              mma_commit(bar(L::kSFull + t));
-            }
-          if (!ok) break;
-          mma_commit(bar(L::kEmpty + s));
-          ++e;
-        }
-        const int s = e % STAGES;
-        ok = mbar_wait(bar(L::kFull + s), (e / STAGES) & 1, args.err, kErrTimeoutTma);
-        if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
-          if (ok && j < nblk[t]) {
+          if (nblk[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(bar(L::kSFull + t));
+          }
+        mma_commit(bar(L::kEmpty + 0));
+      }
+      for (int j = 0; ok && j < nb; ++j) {
+        const int ev = 2 * j + 1, ek = 2 * j + 2;  // ring items of V_j and K_{j+1}
+        const bool next = j + 1 < nb;
+        ok = wait_full(ev) && (!next || wait_full(ek));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (j < nblk[t]) {
             ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, s, j);
+            issue_pv(t, ev % STAGES, j);
             mma_commit(bar(L::kODone + t));
           }
+          if (j + 1 < nblk[t]) {
+            issue_s(t, ek % STAGES);  // in order after P_t V_j, which read these columns
+            mma_commit(bar(L::kSFull + t));
+          }
+        }
         if (!ok) break;
-        mma_commit(bar(L::kEmpty + s));
-        ++e;
+        mma_commit(bar(L::kEmpty + ev % STAGES));
+        if (next) mma_commit(bar(L::kEmpty + ek % STAGES));
       }
       // Every MMA must have finished before TMEM can be released.
       mma_commit(bar(L::kDrain));
@@ -269,8 +246,6 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int h = 0; h < 4; ++h) reg_fence32(sr[h]);
-      tc_fence_before();
-      mbar_arrive(bar(L::kSFree + t));  // S_t may now be overwritten by the next block
 
       float s[128];
 #pragma unroll
@@ -294,35 +269,31 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
       const float alpha = ex2_approx(fmaf(m, c, -mc));  // 0 when m = -inf
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      uint32_t pw[2][32];
 #pragma unroll
       for (int i = 0; i < 128; i += 4) {
-        s[i] = ex2_approx(fmaf(s[i], c, -mc));
-        s[i + 1] = ex2_approx(fmaf(s[i + 1], c, -mc));
-        s[i + 2] = ex2_approx(fmaf(s[i + 2], c, -mc));
-        s[i + 3] = ex2_approx(fmaf(s[i + 3], c, -mc));
-        l0 += s[i];
-        l1 += s[i + 1];
-        l2 += s[i + 2];
-        l3 += s[i + 3];
+        const float p0 = ex2_approx(fmaf(s[i], c, -mc));
+        const float p1 = ex2_approx(fmaf(s[i + 1], c, -mc));
+        const float p2 = ex2_approx(fmaf(s[i + 2], c, -mc));
+        const float p3 = ex2_approx(fmaf(s[i + 3], c, -mc));
+        l0 += p0;
+        l1 += p1;
+        l2 += p2;
+        l3 += p3;
+        pw[i >> 6][(i & 63) >> 1] = pack2<BF16>(p0, p1);
+        pw[i >> 6][((i & 63) >> 1) + 1] = pack2<BF16>(p2, p3);
       }
       l = l * alpha + ((l0 + l1) + (l2 + l3));
 
-      // P_t and O_t are free once the previous P V product has completed.
-      if (j > 0) {
+      // P_t into the first 64 columns of S_t (two 16-bit values per column).
+      tmem_st_32x32b_x32(tS, pw[0]);
+      tmem_st_32x32b_x32(tS + 32, pw[1]);
+      tmem_wait_st();
+      // O_t is rescaled only when the reference moved, after the previous P V is done.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         ok = mbar_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int b = h * 64 + cc * 8;
-          st_shared_v4(sP(t) + h * kPanelBytes + sw128_offset(r, cc), pack2<BF16>(s[b], s[b + 1]),
-                       pack2<BF16>(s[b + 2], s[b + 3]), pack2<BF16>(s[b + 4], s[b + 5]),
-                       pack2<BF16>(s[b + 6], s[b + 7]));
-        }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
@@ -335,7 +306,6 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
         }
         tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::kPFull + t));
       m = m_use;
@@ -411,11 +381,11 @@ cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
                        const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream) {
   switch (d) {
     case 64:
-      return bf16 ? launch_fwd_t<64, 2, 4, true>(q, k, v, o, a, stream)
-                  : launch_fwd_t<64, 2, 4, false>(q, k, v, o, a, stream);
+      return bf16 ? launch_fwd_t<64, 2, 8, true>(q, k, v, o, a, stream)
+                  : launch_fwd_t<64, 2, 8, false>(q, k, v, o, a, stream);
     case 128:
-      return bf16 ? launch_fwd_t<128, 2, 3, true>(q, k, v, o, a, stream)
-                  : launch_fwd_t<128, 2, 3, false>(q, k, v, o, a, stream);
+      return bf16 ? launch_fwd_t<128, 2, 5, true>(q, k, v, o, a, stream)
+                  : launch_fwd_t<128, 2, 5, false>(q, k, v, o, a, stream);
     case 256:
       return bf16 ? launch_fwd_t<256, 1, 2, true>(q, k, v, o, a, stream)
                   : launch_fwd_t<256, 1, 2, false>(q, k, v, o, a, stream);
