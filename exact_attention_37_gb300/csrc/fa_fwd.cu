@@ -209,13 +209,13 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
             issue_pv(t, ev % STAGES, j);
             mma_commit(bar(L::kODone + t));
           }
+          if (t == NQ - 1) mma_commit(bar(L::kEmpty + ev % STAGES));  // last reader of V_j issued
           if (j + 1 < nblk[t]) {
             issue_s(t, ek % STAGES);  // in order after P_t V_j, which read these columns
             mma_commit(bar(L::kSFull + t));
           }
         }
         if (!ok) break;
-        mma_commit(bar(L::kEmpty + ev % STAGES));
         if (next) mma_commit(bar(L::kEmpty + ek % STAGES));
       }
       // Every MMA must have finished before TMEM can be released.
@@ -255,39 +255,43 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (i < nvalid) ? s[i] : -INFINITY;
       }
+      // Row maximum: four independent chains of 3-input max.
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
+      for (int i = 4; i < 124; i += 8) {
+        mx0 = max3f(mx0, s[i], s[i + 1]);
+        mx1 = max3f(mx1, s[i + 2], s[i + 3]);
+        mx2 = max3f(mx2, s[i + 4], s[i + 5]);
+        mx3 = max3f(mx3, s[i + 6], s[i + 7]);
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+      mx0 = max3f(mx0, s[124], s[125]);
+      mx1 = max3f(mx1, s[126], s[127]);
+      const float m_new = max3f(m, max3f(mx0, mx1, mx2), mx3);
       // Keep the old reference unless the maximum grew by more than 8 (base 2).
       const float m_use = (m == -INFINITY || (m_new - m) * c > 8.f) ? m_new : m;
       const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
       const float alpha = ex2_approx(fmaf(m, c, -mc));  // 0 when m = -inf
+      // p = 2^(s c - m c): packed FMA for the exponent, ex2, packed adds for the row
+      // sum.  P goes into the first 64 columns of S_t (two 16-bit values per column),
+      // half a row at a time so the packed words do not all stay live.
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-      uint32_t pw[2][32];
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float p0 = ex2_approx(fmaf(s[i], c, -mc));
-        const float p1 = ex2_approx(fmaf(s[i + 1], c, -mc));
-        const float p2 = ex2_approx(fmaf(s[i + 2], c, -mc));
-        const float p3 = ex2_approx(fmaf(s[i + 3], c, -mc));
-        l0 += p0;
-        l1 += p1;
-        l2 += p2;
-        l3 += p3;
-        pw[i >> 6][(i & 63) >> 1] = pack2<BF16>(p0, p1);
-        pw[i >> 6][((i & 63) >> 1) + 1] = pack2<BF16>(p2, p3);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 64 * h; i < 64 * h + 64; i += 4) {
+          float x0, x1, x2, x3;
+          fma2(s[i], s[i + 1], c, -mc, x0, x1);
+          fma2(s[i + 2], s[i + 3], c, -mc, x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          add2(l0, l1, p0, p1);
+          add2(l2, l3, p2, p3);
+          pw[(i & 63) >> 1] = pack2<BF16>(p0, p1);
+          pw[((i & 63) >> 1) + 1] = pack2<BF16>(p2, p3);
+        }
+        tmem_st_32x32b_x32(tS + 32 * h, pw);
       }
       l = l * alpha + ((l0 + l1) + (l2 + l3));
-
-      // P_t into the first 64 columns of S_t (two 16-bit values per column).
-      tmem_st_32x32b_x32(tS, pw[0]);
-      tmem_st_32x32b_x32(tS + 32, pw[1]);
       tmem_wait_st();
       // O_t is rescaled only when the reference moved, after the previous P V is done.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {

@@ -194,6 +194,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (d0, d1) = (a0 * b + c, a1 * b + c) with one packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float a0, float a1, float b, float c, float& d0, float& d1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n mov.b64 c, {%5, %5};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1) with one packed f32x2 add.
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 a, d;\n mov.b64 a, {%2, %3};\n mov.b64 d, {%0, %1};\n"
+      " add.f32x2 d, d, a;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 // Pack two fp32 values into one 32-bit word of 16-bit values (lo in bits 0-15), round to nearest even.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
