@@ -31,6 +31,7 @@ SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_check_device_status": (_i, [_vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
     "fa_status_string": (ctypes.c_char_p, [_i]),
@@ -127,6 +128,18 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: b
                       _ptr(workspace), ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q),
                       _stream(stream))
     _check("fa_bwd", code)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool, stream=None):
+    """fa_bwd with the library's fixed device scratch instead of a caller workspace (no allocation)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    for t in (q, k, v, o, dout, lse, dq, dk, dv):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    code = lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                              _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check("fa_bwd_noalloc", code)
 
 
 def fa_check_device_status(stream=None):

@@ -228,6 +228,50 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace fa {
+namespace {
+// Fixed scratch of fa_bwd_noalloc (fp32 dQ accumulator + fp32 D rows).  Its
+// name in host code is only a host-side stand-in; the device address comes
+// from cudaGetSymbolAddress on each device.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch on the current device, looked up once per device.
+void* noalloc_scratch_ptr() {
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, fa_dtype dtype, fa_stream_t stream) {
+  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+  if (st != FA_OK) return st;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (fa_bwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  void* scratch = noalloc_scratch_ptr();
+  if (!scratch) return FA_ERR_CUDA;
+  return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes, B, H, N, d, scale, causal, dtype,
+                stream);
+}
+
 fa_status fa_check_device_status(fa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   uint32_t bits = 0;

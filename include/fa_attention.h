@@ -104,6 +104,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * fa_bwd without a caller-provided workspace, for callers that cannot allocate
+ * device memory: code that runs inside another runtime's allocator or memory
+ * pool callbacks, hosts that reserved the whole device memory up front for
+ * their own pool, or real-time loops where cudaMalloc's implicit device
+ * synchronization is not acceptable.  (The attention method itself has no
+ * counterpart to this entry point; it only changes where the scratch lives.)
+ *
+ * Arguments, layout, results and errors are those of fa_bwd, minus the
+ * workspace pair.  The scratch (the fp32 dQ accumulator and the fp32 D rows,
+ * fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
+ * library's device memory, allocated when the library's device code is loaded
+ * and held by every GPU that loads it until the process exits.  Calls whose
+ * scratch would exceed 32 MiB (33554432 bytes) return FA_ERR_WORKSPACE and
+ * launch nothing; with d = 128 that is B*H*N up to 65,027 rows.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.  No
+ * call allocates: no cudaMalloc, cudaFree or allocating library routine.  Every
+ * call overwrites the whole scratch region it uses before reading it (the D
+ * pre-pass zeroes the dQ accumulator), so stale contents from an earlier call
+ * never leak into a result.  All calls share the one array: two calls whose
+ * kernels overlap on the GPU (different streams, no ordering between them)
+ * race on it and give wrong gradients; order them on one stream or with events.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device error word of the
  * current device.  FA_OK if no kernel gave up on a wait since the last check,
  * FA_ERR_DEVICE_TIMEOUT otherwise, FA_ERR_CUDA if the synchronization failed.

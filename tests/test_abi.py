@@ -90,6 +90,15 @@ def test_bwd_rejects_bad_arguments_on_the_host(lib):
     assert bwd(lib, B=0) == 0
 
 
+def test_noalloc_backward_rejects_oversized_problems_on_the_host(lib):
+    vp = ctypes.c_void_p
+    args = [vp(256)] * 9
+    # the fixed scratch holds 32 MiB: d = 128 fits 65,027 rows, not 65,028
+    assert lib.fa_bwd_noalloc(*args, 1, 1, 65028, 128, 0.1, 0, 1, None) == 4
+    assert lib.fa_bwd_noalloc(*args, 1, 1, 8, 96, 0.1, 0, 1, None) == 2
+    assert lib.fa_bwd_noalloc(*args, 0, 1, 8, 64, 0.1, 0, 1, None) == 0
+
+
 def test_workspace_is_linear_in_n(lib):
     sizes = [lib.fa_bwd_workspace_size(2, 16, n, 128) for n in (1024, 2048, 4096, 8192)]
     per_row = (128 + 1) * 4
