@@ -63,18 +63,19 @@ struct BwdLayout {
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kKVTile;
   static constexpr uint32_t kQ = kV + kKVTile;                    // STG stages of (Q, dO)
-  static constexpr uint32_t kPds = kQ + STG * 2 * kQTile;         // NPB x (P^T, dS^T)
-  static constexpr uint32_t pt(int b) { return kPds + 2u * kPdsTile * b; }
-  static constexpr uint32_t dst(int b) { return kPds + 2u * kPdsTile * b + kPdsTile; }
-  static constexpr uint32_t kLD = kPds + 2u * kPdsTile * NPB;     // 2 buffers x (L, D) x BM floats
+  static constexpr uint32_t kDs = kQ + STG * 2 * kQTile;          // NPB x dS^T
+  static constexpr uint32_t dst(int b) { return kDs + kPdsTile * b; }
+  static constexpr uint32_t kLD = kDs + kPdsTile * NPB;           // 2 buffers x (L, D) x BM floats
   static constexpr uint32_t kBar = kLD + 2 * 2 * BM * 4;
   static constexpr int kKVFull = 0;
   static constexpr int kQFull = 1;
   static constexpr int kQEmpty = kQFull + STG;
-  static constexpr int kSFull = kQEmpty + STG;
-  static constexpr int kSdpFree = kSFull + 1;
-  static constexpr int kPdsFull = kSdpFree + 1;                   // two, used alternately
-  static constexpr int kGrads = kPdsFull + 2;                     // one per P^T/dS^T buffer
+  static constexpr int kSReady = kQEmpty + STG;                   // S^T of the block is in TMEM
+  static constexpr int kDpReady = kSReady + 1;                    // dP^T of the block is in TMEM
+  static constexpr int kSdpFree = kDpReady + 1;                   // S^T and dP^T have been read out
+  static constexpr int kPFull = kSdpFree + 1;                     // two, used alternately: P^T in TMEM
+  static constexpr int kDsFull = kPFull + 2;                      // two, used alternately: dS^T in smem
+  static constexpr int kGrads = kDsFull + 2;                      // one per P^T/dS^T buffer
   static constexpr int kDqFree = kGrads + NPB;
   static constexpr int kDrain = kDqFree + 1;
   static constexpr int kNumBars = kDrain + 1;
@@ -88,8 +89,10 @@ struct BwdLayout {
   static constexpr uint32_t kColDK = 2 * BM + DH;
   static constexpr uint32_t kColDQ = 2 * BM + 2 * DH;
   static constexpr uint32_t kDqCols = DQT ? BM : DH;
+  static constexpr uint32_t kColPt = kColDQ + kDqCols;            // NPB x P^T (16-bit pairs, BM/2 columns)
+  static constexpr uint32_t pt_col(int b) { return kColPt + (uint32_t)(BM / 2) * b; }
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColDQ + kDqCols <= 512, "TMEM budget");
+  static_assert(kColPt + NPB * (BM / 2) <= 512, "TMEM budget");
   static_assert(kBytes + 1024 <= 232448, "shared memory budget");
   static_assert(!DQT || DH == 128, "dQ^T needs M = 128");
   static_assert(DQT || BM == 128, "dQ needs M = 128");
@@ -122,7 +125,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sQ = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s; };
   auto sDO = [&](int s) -> uint32_t { return sbase + L::kQ + 2u * L::kQTile * s + L::kQTile; };
   const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
-  auto sPt = [&](int b) -> uint32_t { return sbase + L::pt(b); };
   auto sDSt = [&](int b) -> uint32_t { return sbase + L::dst(b); };
 
   const int warp = threadIdx.x >> 5;
@@ -147,10 +149,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(L::kQFull + s), 1);
       mbar_init(bar(L::kQEmpty + s), 1);
     }
-    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kSReady), 1);
+    mbar_init(bar(L::kDpReady), 1);
     mbar_init(bar(L::kSdpFree), 256);
-    mbar_init(bar(L::kPdsFull + 0), 256);
-    mbar_init(bar(L::kPdsFull + 1), 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kPFull + b), 256);
+      mbar_init(bar(L::kDsFull + b), 256);
+    }
     for (int b = 0; b < NPB; ++b) mbar_init(bar(L::kGrads + b), 1);
     mbar_init(bar(L::kDqFree), 128);
     mbar_init(bar(L::kDrain), 1);
@@ -200,50 +205,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdQ = DQT ? make_idesc_f16(BF16, DH, BM, true, true)   // dQ^T: M=DH, N=BM, A=K^T
                                     : make_idesc_f16(BF16, BM, DH, true, true);  // dQ: M=BM, N=DH, A=dS
       const uint32_t hp = (uint32_t)(half * (DH / 64));  // first 64-column panel of this CTA's half
+      constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand here: 8-row groups 1024 B apart
       auto issue_sdp = [&](int s) {
+        const uint32_t k0 = sdesc_lo(sK, 16), v0 = sdesc_lo(sV, 16);
+        const uint32_t q0 = sdesc_lo(sQ(s), 16), o0 = sdesc_lo(sDO(s), 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kKVPanel + (kk & 3) * 32;
-          const uint32_t b_off = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
-          mma_ss(tmem + L::kColS, make_sdesc_sw128(sK + a_off, 16, 1024), make_sdesc_sw128(sQ(s) + b_off, 16, 1024),
-                 kIdS, kk > 0);
+          const uint32_t a_off = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
+          mma_ss_lohi(tmem + L::kColS, k0 + a_off, kHi, q0 + b_off, kHi, kIdS, kk > 0);
         }
+        mma_commit(bar(L::kSReady));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kKVPanel + (kk & 3) * 32;
-          const uint32_t b_off = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
-          mma_ss(tmem + L::kColDP, make_sdesc_sw128(sV + a_off, 16, 1024),
-                 make_sdesc_sw128(sDO(s) + b_off, 16, 1024), kIdS, kk > 0);
+          const uint32_t a_off = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
+          mma_ss_lohi(tmem + L::kColDP, v0 + a_off, kHi, o0 + b_off, kHi, kIdS, kk > 0);
         }
+        mma_commit(bar(L::kDpReady));
       };
-      auto issue_grads = [&](int s, int it) {
+      // dV += P^T dO: A (P^T) from TMEM, B (dO) MN-major over the DH columns.
+      auto issue_dv = [&](int s, int it) {
         const int pb = it % NPB;
-        // dV += P^T dO, dK += dS^T Q: A K-major over the BM queries, B MN-major (DH columns).
+        const uint32_t o0 = sdesc_lo(sDO(s) + hp * L::kQPanel, L::kQPanel);
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ts_lohi(tmem + L::kColDV, tmem + L::pt_col(pb) + 8 * kk, o0 + ((kk * 2048) >> 4), kHi, kIdG,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+      };
+      // dK += dS^T Q (A K-major from smem), then dQ (or dQ^T) over the block's 128 keys.
+      auto issue_dk_dq = [&](int s, int it) {
+        const int pb = it % NPB;
+        const uint32_t ds0 = sdesc_lo(sDSt(pb), 16), q0 = sdesc_lo(sQ(s) + hp * L::kQPanel, L::kQPanel);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kPdsPanel + (kk & 3) * 32;
-          const uint32_t b_off = hp * L::kQPanel + kk * 2048;
-          mma_ss(tmem + L::kColDV, make_sdesc_sw128(sPt(pb) + a_off, 16, 1024),
-                 make_sdesc_sw128(sDO(s) + b_off, L::kQPanel, 1024), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t a_off = ((kk >> 2) * L::kPdsPanel + (kk & 3) * 32) >> 4;
+          mma_ss_lohi(tmem + L::kColDK, ds0 + a_off, kHi, q0 + ((kk * 2048) >> 4), kHi, kIdG,
+                      (it > 0 || kk > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kPdsPanel + (kk & 3) * 32;
-          const uint32_t b_off = hp * L::kQPanel + kk * 2048;
-          mma_ss(tmem + L::kColDK, make_sdesc_sw128(sDSt(pb) + a_off, 16, 1024),
-                 make_sdesc_sw128(sQ(s) + b_off, L::kQPanel, 1024), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dQ (or dQ^T) over the 128 keys of this block; both operands MN-major.
+        const uint32_t kmn0 = sdesc_lo(sK + hp * L::kKVPanel, L::kKVPanel);
+        const uint32_t dsmn0 = sdesc_lo(sDSt(pb), L::kPdsPanel);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t k_off = hp * L::kKVPanel + kk * 2048;
-          const uint32_t ds_off = kk * 2048;
+          const uint32_t off = (kk * 2048) >> 4;
           if constexpr (DQT) {
-            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024),
-                   make_sdesc_sw128(sDSt(pb) + ds_off, L::kPdsPanel, 1024), kIdQ, kk > 0);
+            mma_ss_lohi(tmem + L::kColDQ, kmn0 + off, kHi, dsmn0 + off, kHi, kIdQ, kk > 0);
           } else {
-            mma_ss(tmem + L::kColDQ, make_sdesc_sw128(sDSt(pb) + ds_off, L::kPdsPanel, 1024),
-                   make_sdesc_sw128(sK + k_off, L::kKVPanel, 1024), kIdQ, kk > 0);
+            mma_ss_lohi(tmem + L::kColDQ, dsmn0 + off, kHi, kmn0 + off, kHi, kIdQ, kk > 0);
           }
         }
       };
@@ -252,7 +260,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(bar(L::kQFull + s1), ((it + 1) / STG) & 1, args.err, kErrTimeoutTma)) return false;
         tc_fence_after();
         issue_sdp(s1);
-        mma_commit(bar(L::kSFull));
         return true;
       };
       bool ok = mbar_wait(bar(L::kKVFull), 0, args.err, kErrTimeoutTma);
@@ -260,7 +267,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_sdp(0);
-        mma_commit(bar(L::kSFull));
       }
       for (int it = 0; ok && it < nit; ++it) {
         const int s = it % STG;
@@ -272,15 +278,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait(bar(L::kSdpFree), it & 1, args.err, kErrTimeoutSoftmax);
           if (!ok || !(ok = next_scores(it))) break;
         }
-        ok = mbar_wait(bar(L::kPdsFull + (it & 1)), (it >> 1) & 1, args.err, kErrTimeoutSoftmax);
+        ok = mbar_wait(bar(L::kPFull + (it & 1)), (it >> 1) & 1, args.err, kErrTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        if (it > 0) {
-          ok = mbar_wait(bar(L::kDqFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        issue_grads(s, it);
+        issue_dv(s, it);
+        ok = mbar_wait(bar(L::kDsFull + (it & 1)), (it >> 1) & 1, args.err, kErrTimeoutSoftmax);
+        if (!ok) break;
+        if (it > 0) ok = mbar_wait(bar(L::kDqFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dk_dq(s, it);
         mma_commit(bar(L::kGrads + it % NPB));
         mma_commit(bar(L::kQEmpty + s));
         if (STG == 1 && it + 1 < nit && !(ok = next_scores(it))) break;
@@ -323,78 +330,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       prefetch(it + 1);
       named_bar_sync(1 + e, 128);
-      if (!mbar_wait(bar(L::kSFull), it & 1, args.err, kErrTimeoutMma)) break;
-      tc_fence_after();
       const bool diag = args.causal && (key0 + kBN - 1 > q0);  // some key of the block is after some query
       const int pb = it % NPB;
-      // The P^T/dS^T buffer pb is free once the gradients of block it-NPB (its last reader) are done.
-      auto wait_buffer = [&]() -> bool {
-        if (it < NPB) return true;
-        if (!mbar_wait(bar(L::kGrads + pb), ((it / NPB) - 1) & 1, args.err, kErrTimeoutMma)) return false;
+      // P^T of block it-NPB (TMEM buffer pb) and dS^T (smem buffer pb) are free once
+      // that block's gradients are done.
+      if (it >= NPB) {
+        if (!mbar_wait(bar(L::kGrads + pb), ((it / NPB) - 1) & 1, args.err, kErrTimeoutMma)) break;
         tc_fence_after();
-        return true;
-      };
-      uint32_t pw[kCW / 2], dw[kCW / 2];
-      bool ok = true;
-      if constexpr (kNCh > 1) ok = wait_buffer();  // wide blocks write chunk by chunk
-      if (!ok) break;
+      }
+      // ---- P^T = 2^(S^T c - L log2 e), as soon as S^T is in TMEM (dP^T may still be running)
+      if (!mbar_wait(bar(L::kSReady), it & 1, args.err, kErrTimeoutMma)) break;
+      tc_fence_after();
+      float p[kCW];
 #pragma unroll
       for (int ch = 0; ch < kNCh; ++ch) {
-        uint32_t sv[32], dv[32];
+        uint32_t sv[32];
         tmem_ld_32x32b_x32(tmem + lane_base + L::kColS + cbeg + 32 * ch, sv);
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + cbeg + 32 * ch, dv);
         tmem_wait_ld();
         reg_fence32(sv);
-        reg_fence32(dv);
-        if (ch == kNCh - 1) {
-          tc_fence_before();  // this thread is done reading S^T and dP^T from TMEM
-          mbar_arrive(bar(L::kSdpFree));
-        }
-        float p[32], ds[32];
+        uint32_t pw[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const int col = cbeg + 32 * ch + 4 * e4;
           const float4 l4 = *reinterpret_cast<const float4*>(bufL + col);
-          const float4 d4 = *reinterpret_cast<const float4*>(bufD + col);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int x = 4 * e4 + u;
             float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lv[u]));
             if (diag && key > q0 + col + u) pe = 0.f;
-            p[x] = pe;
-            ds[x] = pe * (__uint_as_float(dv[x]) - dd[u]);
+            p[32 * ch + x] = pe;
           }
         }
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          pw[16 * ch + x] = pack2<BF16>(p[2 * x], p[2 * x + 1]);
-          dw[16 * ch + x] = pack2<BF16>(ds[2 * x], ds[2 * x + 1]);
-        }
-        if constexpr (kNCh > 1) {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int chunk = (cbeg + 32 * ch) / 8 + k4;  // 16-byte chunk index along the row
-            const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
-            const int w = 16 * ch + 4 * k4;
-            st_shared_v4(sPt(pb) + off, pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
-            st_shared_v4(sDSt(pb) + off, dw[w], dw[w + 1], dw[w + 2], dw[w + 3]);
-          }
-        }
+        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[32 * ch + 2 * x], p[32 * ch + 2 * x + 1]);
+        tmem_st_32x32b_x16(tmem + lane_base + L::pt_col(pb) + (cbeg + 32 * ch) / 2, pw);
       }
-      if constexpr (kNCh == 1) {
-        if (!wait_buffer()) break;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + (it & 1)));
+      // ---- dS^T = P^T o (dP^T - D)
+      if (!mbar_wait(bar(L::kDpReady), it & 1, args.err, kErrTimeoutMma)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < kNCh; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kColDP + cbeg + 32 * ch, dv);
+        tmem_wait_ld();
+        reg_fence32(dv);
+        if (ch == kNCh - 1) {
+          tc_fence_before();  // this thread is done reading S^T and dP^T from TMEM
+          mbar_arrive(bar(L::kSdpFree));
+        }
+        uint32_t dw[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int col = cbeg + 32 * ch + 4 * e4;
+          const float4 d4 = *reinterpret_cast<const float4*>(bufD + col);
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            const int x = 4 * e4 + u;
+            const float ds0 = p[32 * ch + x] * (__uint_as_float(dv[x]) - dd[u]);
+            const float ds1 = p[32 * ch + x + 1] * (__uint_as_float(dv[x + 1]) - dd[u + 1]);
+            dw[x >> 1] = pack2<BF16>(ds0, ds1);
+          }
+        }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const int chunk = cbeg / 8 + k4;
+          const int chunk = (cbeg + 32 * ch) / 8 + k4;  // 16-byte chunk index along the row
           const uint32_t off = (chunk >> 3) * L::kPdsPanel + sw128_offset(r, chunk & 7);
-          st_shared_v4(sPt(pb) + off, pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
           st_shared_v4(sDSt(pb) + off, dw[4 * k4], dw[4 * k4 + 1], dw[4 * k4 + 2], dw[4 * k4 + 3]);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(L::kPdsFull + (it & 1)));
+      mbar_arrive(bar(L::kDsFull + (it & 1)));
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain + dK/dV epilogue

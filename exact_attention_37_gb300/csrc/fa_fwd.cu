@@ -166,19 +166,21 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_f16(BF16, kBM, kBN, false, false);
       constexpr uint32_t kIdPV = make_idesc_f16(BF16, kBM, D, false, true);
+      constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand here: 8-row groups 1024 B apart
       auto issue_s = [&](int t, int s) {
+        const uint32_t a0 = sdesc_lo(sQ(t), 16), b0 = sdesc_lo(sRing(s), 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + L::s_col(t), make_sdesc_sw128(sQ(t) + off, 16, 1024),
-                 make_sdesc_sw128(sRing(s) + off, 16, 1024), kIdS, kk > 0);
+          const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lohi(tmem + L::s_col(t), a0 + off, kHi, b0 + off, kHi, kIdS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, int j) {
+        const uint32_t b0 = sdesc_lo(sRing(s), kPanelBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)  // P_t: 8 TMEM columns (16 keys) per step
-          mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + 8 * kk,
-                 make_sdesc_sw128(sRing(s) + kk * 2048, kPanelBytes, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_lohi(tmem + L::o_col(t), tmem + L::s_col(t) + 8 * kk, b0 + ((kk * 2048) >> 4), kHi, kIdPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
       };
       auto wait_full = [&](int e) -> bool {
         return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
