@@ -52,7 +52,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // DQT: compute dQ^T (M = DH) instead of dQ (M = BM); STG: Q/dO pipeline depth;
 // NPB: P^T/dS^T tile buffers (2 lets the softmax warps write block i+1 while the
 // tensor cores still read block i).
-template <int D, int DH, int BM, bool DQT, int STG, int NPB>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB>
 struct BwdLayout {
   static constexpr uint32_t kKVPanel = kBN * 128;                 // 128 key rows x 128 B
   static constexpr uint32_t kQPanel = BM * 128;                   // BM query rows x 128 B
@@ -66,7 +66,11 @@ struct BwdLayout {
   static constexpr uint32_t kDs = kQ + STG * 2 * kQTile;          // NPB x dS^T
   static constexpr uint32_t dst(int b) { return kDs + kPdsTile * b; }
   static constexpr uint32_t kLD = kDs + kPdsTile * NPB;           // 2 buffers x (L, D) x BM floats
-  static constexpr uint32_t kBar = kLD + 2 * 2 * BM * 4;
+  // dQ staging (DQB, with dQ^T): BM query rows of DH fp32, transposed through shared
+  // memory so the accumulation can use 128-bit reductions.
+  static constexpr uint32_t kDqRowBytes = DH * 4;
+  static constexpr uint32_t kDqStage = kLD + 2 * 2 * BM * 4;
+  static constexpr uint32_t kBar = kDqStage + (DQB ? BM * kDqRowBytes : 0);
   static constexpr int kKVFull = 0;
   static constexpr int kQFull = 1;
   static constexpr int kQEmpty = kQFull + STG;
@@ -105,16 +109,19 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 __device__ __forceinline__ void red_add(float* addr, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdArgs args) {
-  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
   constexpr int kHalves = D / DH;
   constexpr int kCW = BM / 2;        // query columns per elementwise warpgroup
   constexpr int kNCh = kCW / 32;     // 32-column TMEM chunks per elementwise thread
@@ -427,7 +434,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int ch = 0; ch < kCh; ++ch) reg_fence32(v[ch]);
       tc_fence_before();
       mbar_arrive(bar(L::kDqFree));
-      if constexpr (DQT) {
+      if constexpr (DQB && DQT) {
+        // dQ^T gives each lane one column of the block's dQ rows.  Transpose it
+        // through shared memory so every thread then owns 16-byte pieces of rows
+        // and the accumulation uses 128-bit reductions (a quarter of the
+        // instructions of per-column ones).
+        const uint32_t stg = sbase + L::kDqStage;
+        named_bar_sync(3, 128);  // the previous block's staged rows have been read
+#pragma unroll
+        for (int ch = 0; ch < kCh; ++ch)
+#pragma unroll
+          for (int x = 0; x < 32; ++x) st_shared_f32(stg + (32 * ch + x) * L::kDqRowBytes + 4 * r, v[ch][x]);
+        named_bar_sync(3, 128);
+        constexpr int kV4PerRow = DH / 4;
+#pragma unroll 4
+        for (int j = r; j < BM * kV4PerRow; j += 128) {
+          const int row = j / kV4PerRow, c4 = j % kV4PerRow;
+          if (q0 + row < N) {
+            uint32_t a0, a1, a2, a3;
+            ld_shared_v4(stg + row * L::kDqRowBytes + 16 * c4, a0, a1, a2, a3);
+            red_add_v4(dq_acc + (size_t)(q0 + row) * D + half * DH + 4 * c4, __uint_as_float(a0),
+                       __uint_as_float(a1), __uint_as_float(a2), __uint_as_float(a3));
+          }
+        }
+      } else if constexpr (DQT) {
         // lane r holds dQ^T row r: column half*DH + r of query rows q0 .. q0+BM-1
         const int col = half * DH + r;
 #pragma unroll
@@ -538,10 +568,10 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const BwdArgs ar
   }
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
 cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                          const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -556,7 +586,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   }
   // 2) main kernel
   {
-    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, BF16>;
+    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, DQB, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
     if (e != cudaSuccess) return e;
     const long long nkb = (a.N + kBN - 1) / kBN;
@@ -584,14 +614,14 @@ cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
     case 64:
-      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, 1, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<64, 64, 128, false, 3, 1, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, 1, false, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<64, 64, 128, false, 3, 1, false, false>(q, k, v, dout, a, stream);
     case 128:
-      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, 2, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<128, 128, 64, true, 3, 2, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, 2, true, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<128, 128, 64, true, 3, 2, true, false>(q, k, v, dout, a, stream);
     case 256:
-      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, 1, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<256, 128, 64, true, 1, 1, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, 1, false, true>(q, k, v, dout, a, stream)
+                  : launch_bwd_t<256, 128, 64, true, 1, 1, false, false>(q, k, v, dout, a, stream);
     default:
       return cudaErrorInvalidValue;
   }
