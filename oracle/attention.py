@@ -26,6 +26,16 @@ What it follows
   "Performance and efficiency"), so a gradient exists; these are the standard
   chain-rule derivatives of softmax, written out.
 
+Extensions (the "next" rows of the build, readings of the pages' MQA support --
+page "FlashAttention — فلاش أتنشن", section "FlashAttention-2" -- and of the
+causal mask for unequal lengths):
+* Grouped / multi-query attention: K and V carry H_kv heads, H_kv divides H, and
+  query head h attends to key/value head h // (H / H_kv).  H_kv = 1 is multi-query
+  attention, H_kv = H plain multi-head attention.
+* Unequal lengths: Q has N_q rows, K and V have N_k rows.  Under the causal mask
+  key j is visible to query i iff j <= i + (N_k - N_q) (the last query row sees
+  every key).  A row that sees no key has O = 0 and L = -inf.
+
 Pins (tests/test_oracle.py): rows of P sum to 1; a blockwise online softmax
 written independently in the tests equals this two-pass softmax; constant V
 rows reproduce the constant; causal row 0 attends to key 0 only; Q = 0 gives
@@ -58,38 +68,57 @@ def _f64(x) -> np.ndarray:
 def scores(q_h, k_h, scale: float, causal: bool, rows=None) -> np.ndarray:
     """S = scale * q k^T for one head, with -inf where the causal mask hides key j from query i.
 
-    ``rows`` selects query rows (their absolute indices decide the mask).
+    ``rows`` selects query rows (their absolute indices decide the mask).  With N_q
+    query rows and N_k keys the mask is aligned at the bottom right: key j is
+    visible to query i iff j <= i + N_k - N_q.
     """
     q_h = _f64(q_h)
     k_h = _f64(k_h)
     idx = np.arange(q_h.shape[0]) if rows is None else np.asarray(rows)
     S = float(scale) * (q_h[idx] @ k_h.T)
     if causal:
+        shift = k_h.shape[0] - q_h.shape[0]
         keys = np.arange(k_h.shape[0])
-        S = np.where(keys[None, :] > idx[:, None], -np.inf, S)
+        S = np.where(keys[None, :] > idx[:, None] + shift, -np.inf, S)
     return S
 
 
 def probabilities(S: np.ndarray):
-    """Row softmax of S by the two-pass textbook form; returns (P, L) with L the natural logsumexp."""
+    """Row softmax of S by the two-pass textbook form; returns (P, L) with L the natural logsumexp.
+
+    A row whose scores are all -inf (no visible key) gets P = 0 and L = -inf.
+    """
     M = S.max(axis=1, keepdims=True)
-    E = np.exp(S - M)
+    empty = ~np.isfinite(M)
+    Msafe = np.where(empty, 0.0, M)
+    E = np.exp(S - Msafe)
     l = E.sum(axis=1, keepdims=True)
-    P = E / l
-    L = (M + np.log(l))[:, 0]
+    P = np.where(empty, 0.0, E / np.where(empty, 1.0, l))
+    with np.errstate(divide="ignore"):
+        L = np.where(empty, -np.inf, Msafe + np.log(l))[:, 0]
     return P, L
 
 
+def kv_head(h: int, H: int, H_kv: int) -> int:
+    """Key/value head that query head h reads under grouped-query attention."""
+    return h // (H // H_kv)
+
+
 def attention_forward(q, k, v, scale: float, causal: bool):
-    """O [B,H,N,d] and L [B,H,N] in float64, one head at a time, S and P materialised."""
+    """O [B,H,N_q,d] and L [B,H,N_q] in float64, one head at a time, S and P materialised.
+
+    k and v are [B,H_kv,N_k,d]; H_kv divides H (grouped-query attention).
+    """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
-    O = np.empty((B, H, N, d))
+    H_kv = k.shape[1]
+    O = np.empty((B, H, N, v.shape[3]))
     L = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
-            P, Lh = probabilities(scores(q[b, h], k[b, h], scale, causal))
-            O[b, h] = P @ v[b, h]
+            g = kv_head(h, H, H_kv)
+            P, Lh = probabilities(scores(q[b, h], k[b, g], scale, causal))
+            O[b, h] = P @ v[b, g]
             L[b, h] = Lh
     return O, L
 
@@ -107,17 +136,25 @@ def _head_backward(q_h, k_h, v_h, do_h, scale, causal):
 
 
 def attention_backward(q, k, v, dout, scale: float, causal: bool):
-    """dQ, dK, dV [B,H,N,d] and D [B,H,N] in float64 for the loss sum(O o dout)."""
+    """dQ [B,H,N_q,d], dK and dV [B,H_kv,N_k,d], D [B,H,N_q] in float64 for the loss sum(O o dout).
+
+    Under grouped-query attention a key/value head's gradient is the sum of the
+    gradients it receives from every query head of its group.
+    """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, H, N, d = q.shape
+    H_kv = k.shape[1]
     dQ = np.empty_like(q)
-    dK = np.empty_like(k)
-    dV = np.empty_like(v)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(v)
     D = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
-            dQ[b, h], dK[b, h], dV[b, h], D[b, h] = _head_backward(
-                q[b, h], k[b, h], v[b, h], dout[b, h], float(scale), causal)
+            g = kv_head(h, H, H_kv)
+            dq, dk, dv, D[b, h] = _head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], float(scale), causal)
+            dQ[b, h] = dq
+            dK[b, g] += dk
+            dV[b, g] += dv
     return dQ, dK, dV, D
 
 

@@ -339,3 +339,103 @@ def test_planted_mistakes_are_caught(monkeypatch, target, mutant):
         except Exception:
             results = [False]
     assert not all(results), f"planted mistake in {target} went unnoticed"
+
+
+# ----------------------------------------------------------------------------
+# grouped-query attention and unequal lengths (bottom-right causal mask)
+# ----------------------------------------------------------------------------
+
+def gqa_inputs(B=2, H=6, H_kv=2, Nq=19, Nk=23, d=8, seed=71):
+    q = rnd((B, H, Nq, d), seed)
+    k = rnd((B, H_kv, Nk, d), seed + 1)
+    v = rnd((B, H_kv, Nk, d), seed + 2)
+    do = rnd((B, H, Nq, d), seed + 3)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H_kv", [1, 2, 3, 6])
+def test_gqa_equals_repeated_heads(causal, H_kv):
+    """A key/value head shared by a group equals giving every query head its own copy."""
+    q, k, v, do = gqa_inputs(H=6, H_kv=H_kv)
+    G = 6 // H_kv
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    O, L = oracle.attention_forward(q, k, v, 0.4, causal)
+    O2, L2 = oracle.attention_forward(q, kr, vr, 0.4, causal)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+    dq, dk, dv, _ = oracle.attention_backward(q, k, v, do, 0.4, causal)
+    dq2, dk2, dv2, _ = oracle.attention_backward(q, kr, vr, do, 0.4, causal)
+    assert np.abs(dq - dq2).max() < 1e-13
+    assert np.abs(dk - dk2.reshape(2, H_kv, G, 23, 8).sum(axis=2)).max() < 1e-12
+    assert np.abs(dv - dv2.reshape(2, H_kv, G, 23, 8).sum(axis=2)).max() < 1e-12
+
+
+def test_unequal_lengths_causal_rows_match_square_causal():
+    """N_q < N_k: row i sees keys 0..i+(N_k-N_q), i.e. row i+shift of a square causal problem."""
+    Nq, Nk, d = 7, 20, 8
+    q = rnd((1, 1, Nq, d), 81)
+    k, v = rnd((1, 1, Nk, d), 82), rnd((1, 1, Nk, d), 83)
+    O, L = oracle.attention_forward(q, k, v, 0.5, True)
+    qs = np.zeros((1, 1, Nk, d))
+    qs[0, 0, Nk - Nq:] = q[0, 0]
+    Os, Ls = oracle.attention_forward(qs, k, v, 0.5, True)
+    assert np.abs(O[0, 0] - Os[0, 0, Nk - Nq:]).max() < 1e-14
+    assert np.abs(L[0, 0] - Ls[0, 0, Nk - Nq:]).max() < 1e-14
+
+
+def test_more_queries_than_keys_leaves_leading_rows_empty():
+    """N_q > N_k: the first N_q-N_k rows see no key (O = 0, L = -inf); the rest are square causal."""
+    Nq, Nk, d = 12, 5, 4
+    q = rnd((1, 1, Nq, d), 91)
+    k, v = rnd((1, 1, Nk, d), 92), rnd((1, 1, Nk, d), 93)
+    O, L = oracle.attention_forward(q, k, v, 0.5, True)
+    assert np.all(O[0, 0, :Nq - Nk] == 0) and np.all(np.isneginf(L[0, 0, :Nq - Nk]))
+    Os, Ls = oracle.attention_forward(q[:, :, Nq - Nk:], k, v, 0.5, True)
+    assert np.abs(O[0, 0, Nq - Nk:] - Os[0, 0]).max() < 1e-14
+    assert np.abs(L[0, 0, Nq - Nk:] - Ls[0, 0]).max() < 1e-14
+    dq, dk, dv, _ = oracle.attention_backward(q, k, v, rnd((1, 1, Nq, d), 94), 0.5, True)
+    assert np.all(dq[0, 0, :Nq - Nk] == 0)
+
+
+def test_single_query_row_sees_every_key_under_the_mask():
+    q = rnd((1, 1, 1, 8), 101)
+    k, v = rnd((1, 1, 30, 8), 102), rnd((1, 1, 30, 8), 103)
+    Oc, Lc = oracle.attention_forward(q, k, v, 0.3, True)
+    On, Ln = oracle.attention_forward(q, k, v, 0.3, False)
+    assert np.array_equal(Oc, On) and np.array_equal(Lc, Ln)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(9, 14), (14, 9)])
+def test_gqa_unequal_lengths_against_torch_autograd(causal, Nq, Nk):
+    q, k, v, do = gqa_inputs(B=1, H=4, H_kv=2, Nq=Nq, Nk=Nk, d=6, seed=111)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    kr, vr = tk.repeat_interleave(2, dim=1), tv.repeat_interleave(2, dim=1)
+    s = torch.matmul(tq, kr.transpose(-1, -2)) * 0.35
+    if causal:
+        s = s.masked_fill(torch.ones(Nq, Nk, dtype=torch.bool).triu(Nk - Nq + 1), float("-inf"))
+    p = torch.softmax(s, dim=-1).nan_to_num(0.0)  # rows with no visible key: P = 0
+    o = torch.matmul(p, vr)
+    (o * torch.tensor(do)).sum().backward()
+    O, _ = oracle.attention_forward(q, k, v, 0.35, causal)
+    dq, dk, dv, _ = oracle.attention_backward(q, k, v, do, 0.35, causal)
+    assert np.abs(O - o.detach().numpy()).max() < 1e-12
+    for a, b in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert np.abs(a - b.numpy()).max() < 1e-12
+
+
+def test_gqa_unequal_lengths_finite_differences():
+    q, k, v, do = gqa_inputs(B=1, H=2, H_kv=1, Nq=5, Nk=7, d=3, seed=121)
+    h = 1e-6
+    grads = oracle.attention_backward(q, k, v, do, 0.7, True)[:3]
+    for which, g in enumerate(grads):
+        num = np.zeros_like(g)
+        for idx in np.ndindex(*g.shape):
+            plus = [x.copy() for x in (q, k, v)]
+            minus = [x.copy() for x in (q, k, v)]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fp = (oracle.attention_forward(*plus, 0.7, True)[0] * do).sum()
+            fm = (oracle.attention_forward(*minus, 0.7, True)[0] * do).sum()
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.abs(num - g).max() / np.abs(num).max() < 1e-6
