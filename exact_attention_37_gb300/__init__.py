@@ -2,8 +2,11 @@
 softmax and a key-block-parallel backward, behind a small C ABI.
 
     import exact_attention_37_gb300 as fa
-    o, lse = fa.forward(q, k, v, causal=True)          # q, k, v: [B, H, N, d] fp16/bf16 CUDA
+    o, lse = fa.forward(q, k, v, causal=True)          # q: [B, H, N_q, d], k, v: [B, H_kv, N_k, d]
     dq, dk, dv = fa.backward(q, k, v, o, lse, dout, causal=True)
+
+H_kv may be smaller than H (grouped-query / multi-query attention) and N_k may
+differ from N_q (the causal mask is then aligned at the bottom right).
 
 ``forward``/``backward`` allocate their outputs with torch and call the C ABI;
 ``fa_fwd``/``fa_bwd`` take caller-owned outputs.  All compute runs in the

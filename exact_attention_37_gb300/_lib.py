@@ -29,8 +29,11 @@ FA_FP16, FA_BF16 = 0, 1
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                       _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_check_device_status": (_i, [_vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
@@ -99,16 +102,28 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _check_shapes(q, k, v):
+    B, H, Nq, d = _shape(q)
+    Bk, Hkv, Nk, dk = _shape(k)
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or dk != d:
+        raise ValueError("k and v must be [B, H_kv, N_k, d] with q's B and d")
+    if Hkv < 1 or H % Hkv:
+        raise ValueError("the key/value head count must divide the query head count")
+    return B, H, Hkv, Nq, Nk, d
+
+
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):
-    """O and L into caller-owned ``o`` [B,H,N,d] and ``lse`` [B,H,N] fp32 (all CUDA, contiguous)."""
+    """O and L into caller-owned ``o`` [B,H,N_q,d] and ``lse`` [B,H,N_q] fp32 (all CUDA, contiguous).
+
+    k, v: [B, H_kv, N_k, d] (H_kv divides H; N_k may differ from N_q)."""
     lib = load()
-    B, H, N, d = _shape(q)
+    B, H, Hkv, Nq, Nk, d = _check_shapes(q, k, v)
     for t in (q, k, v, o, lse):
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-    code = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
-                      _dtype_code(q), _stream(stream))
-    _check("fa_fwd", code)
+    code = lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk, d, float(scale),
+                         int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check("fa_fwd_ex", code)
 
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
@@ -117,17 +132,17 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None):
     """dQ, dK, dV into caller-owned tensors; ``workspace`` is a CUDA uint8 tensor of at least
-    fa_bwd_workspace_size bytes."""
+    fa_bwd_workspace_size(B, H, N_q, d) bytes."""
     lib = load()
-    B, H, N, d = _shape(q)
+    B, H, Hkv, Nq, Nk, d = _check_shapes(q, k, v)
     for t in (q, k, v, o, dout, lse, dq, dk, dv):
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    code = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                      _ptr(workspace), ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q),
-                      _stream(stream))
-    _check("fa_bwd", code)
+    code = lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                         _ptr(workspace), ws_bytes, B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                         _dtype_code(q), _stream(stream))
+    _check("fa_bwd_ex", code)
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool, stream=None):

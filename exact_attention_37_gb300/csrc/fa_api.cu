@@ -60,16 +60,19 @@ uint32_t* error_word_ptr() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks shared by both passes.  Returns FA_OK or the first problem found.
-fa_status check_common(int B, int H, int N, int d, float scale, int dtype) {
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+fa_status check_common(int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int dtype) {
+  if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
   const long long BH = (long long)B * H;
   // grid size and 32-bit index limits of the kernels
-  if (BH > (1LL << 24) || N > (1 << 28)) return FA_ERR_UNSUPPORTED;
-  const long long fwd_ctas = BH * ((N + 127) / 128);
-  if (fwd_ctas * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (BH > (1LL << 24) || Nq > (1 << 28) || Nk > (1 << 28)) return FA_ERR_UNSUPPORTED;
+  if (BH * ((Nq + 127) / 128) * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H_kv * ((Nk + 127) / 128) * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  // Queries with an empty key set are not a supported problem.
+  if (BH * Nq > 0 && Nk == 0) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -149,26 +152,29 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
-  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                    int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  fa_status st = check_common(B, H, H_kv, N_q, N_k, d, scale, (int)dtype);
   if (st != FA_OK) return st;
-  if ((long long)B * H * N == 0) return FA_OK;  // empty problem
+  if ((long long)B * H * N_q == 0) return FA_OK;  // empty problem
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
   if ((st = check_device()) != FA_OK) return st;
   const bool bf16 = dtype == FA_BF16;
-  const long long BH = (long long)B * H;
+  const long long BH = (long long)B * H, BHkv = (long long)B * H_kv;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, q, BH, N, d, bf16, 128) || !make_map(&mk, k, BH, N, d, bf16, 128) ||
-      !make_map(&mv, v, BH, N, d, bf16, 128) || !make_map(&mo, o, BH, N, d, bf16, 128))
+  if (!make_map(&mq, q, BH, N_q, d, bf16, 128) || !make_map(&mk, k, BHkv, N_k, d, bf16, 128) ||
+      !make_map(&mv, v, BHkv, N_k, d, bf16, 128) || !make_map(&mo, o, BH, N_q, d, bf16, 128))
     return FA_ERR_CUDA;
   FwdArgs a{};
   a.lse = lse;
-  a.N = N;
+  a.N = N_q;
+  a.Nk = N_k;
   a.BH = (int)BH;
+  a.H = H;
+  a.group = H / H_kv;
   const int rows = fwd_rows_per_cta(d);
-  a.num_qblocks = (N + rows - 1) / rows;
+  a.num_qblocks = (N_q + rows - 1) / rows;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
@@ -178,35 +184,49 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, causal, dtype, stream);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (check_common(B, H, N, d, 1.f, FA_FP16) != FA_OK) return 0;
+  if (check_common(B, H, H > 0 ? 1 : 0, N, N, d, 1.f, FA_FP16) != FA_OK) return 0;
   const size_t rows = (size_t)B * H * N;
   if (rows == 0) return 0;
   return round_up(rows * d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
-  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                    int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  fa_status st = check_common(B, H, H_kv, N_q, N_k, d, scale, (int)dtype);
   if (st != FA_OK) return st;
-  if ((long long)B * H * N == 0) return FA_OK;
+  if ((long long)B * H * N_q == 0) {
+    // No query rows: nothing flows back, so dK = dV = 0.
+    const size_t kv_bytes = (size_t)B * H_kv * N_k * d * 2;
+    if (kv_bytes == 0) return FA_OK;
+    if (!dk || !dv) return FA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dk, 0, kv_bytes, s) != cudaSuccess || cudaMemsetAsync(dv, 0, kv_bytes, s) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  const size_t need = fa_bwd_workspace_size(B, H, N_q, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
   if ((st = check_device()) != FA_OK) return st;
   const bool bf16 = dtype == FA_BF16;
-  const long long BH = (long long)B * H;
+  const long long BH = (long long)B * H, BHkv = (long long)B * H_kv;
   const int bm = bwd_query_rows(d);
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_map(&mq, q, BH, N, d, bf16, bm) || !make_map(&mk, k, BH, N, d, bf16, 128) ||
-      !make_map(&mv, v, BH, N, d, bf16, 128) || !make_map(&mdo, dout, BH, N, d, bf16, bm))
+  if (!make_map(&mq, q, BH, N_q, d, bf16, bm) || !make_map(&mk, k, BHkv, N_k, d, bf16, 128) ||
+      !make_map(&mv, v, BHkv, N_k, d, bf16, 128) || !make_map(&mdo, dout, BH, N_q, d, bf16, bm))
     return FA_ERR_CUDA;
-  const size_t rows = (size_t)BH * N;
+  const size_t rows = (size_t)BH * N_q;
   BwdArgs a{};
   a.o = o;
   a.dout = dout;
@@ -216,9 +236,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.N = N;
+  a.N = N_q;
+  a.Nk = N_k;
   a.d = d;
   a.BH = (int)BH;
+  a.BHkv = (int)BHkv;
+  a.H = H;
+  a.group = H / H_kv;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
@@ -226,6 +250,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!a.err) return FA_ERR_CUDA;
   cudaError_t e = launch_bwd(d, bf16, mq, mk, mv, mdo, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, N, d, scale, causal,
+                   dtype, stream);
 }
 
 }  // extern "C"
@@ -260,7 +291,7 @@ extern "C" {
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, fa_dtype dtype, fa_stream_t stream) {
-  fa_status st = check_common(B, H, N, d, scale, (int)dtype);
+  fa_status st = check_common(B, H, H, N, N, d, scale, (int)dtype);
   if (st != FA_OK) return st;
   if ((long long)B * H * N == 0) return FA_OK;
   if (fa_bwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;

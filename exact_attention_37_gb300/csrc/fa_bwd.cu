@@ -140,15 +140,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // Work tile: the lowest key blocks first across all heads (under the causal mask
   // they have the most query blocks), so the last wave holds the lightest work.
-  const int tiles_per_kb = args.BH * kHalves;
+  // One CTA per (key/value head, key block, column half); it visits the query
+  // blocks of every query head of its group, so dK and dV of a shared key/value
+  // head are summed in TMEM without any cross-CTA reduction.
+  const int tiles_per_kb = args.BHkv * kHalves;
   const int kb = (int)(blockIdx.x / tiles_per_kb);
   const int rem = (int)(blockIdx.x % tiles_per_kb);
-  const int bh = rem / kHalves;
+  const int bh_kv = rem / kHalves;
   const int half = rem % kHalves;
+  const int Nk = args.Nk;
+  const int koff = Nk - N;  // causal mask: key j visible to query i iff j <= i + koff
   const int key0 = kb * kBN;
   const int nqb = (N + BM - 1) / BM;
-  const int i_begin = args.causal ? key0 / BM : 0;
-  const int nit = nqb - i_begin;  // query blocks this CTA visits (>= 1)
+  const int i_begin = args.causal ? max(0, key0 - koff) / BM : 0;
+  const int nit_h = nqb - i_begin;    // query blocks per query head (>= 1)
+  const int nit = nit_h * args.group;  // over the whole group
+  const int h_kv = bh_kv % (args.H / args.group);
+  const int bh_q0 = (bh_kv / (args.H / args.group)) * args.H + h_kv * args.group;  // first query head of the group
+  // query head and query block of iteration it
+  auto q_head = [&](int it) { return bh_q0 + it / nit_h; };
+  auto q_block = [&](int it) { return i_begin + it % nit_h; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kKVFull), 1);
@@ -189,18 +200,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_expect_tx(bar(L::kKVFull), 2 * L::kKVTile);
 #pragma unroll
       for (int p = 0; p < D / 64; ++p) {
-        tma_load_3d(sK + p * L::kKVPanel, &tm_k, bar(L::kKVFull), 64 * p, key0, bh);
-        tma_load_3d(sV + p * L::kKVPanel, &tm_v, bar(L::kKVFull), 64 * p, key0, bh);
+        tma_load_3d(sK + p * L::kKVPanel, &tm_k, bar(L::kKVFull), 64 * p, key0, bh_kv);
+        tma_load_3d(sV + p * L::kKVPanel, &tm_v, bar(L::kKVFull), 64 * p, key0, bh_kv);
       }
       for (int it = 0; it < nit; ++it) {
         const int s = it % STG, u = it / STG;
         if (u > 0 && !mbar_wait(bar(L::kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(L::kQFull + s), 2 * L::kQTile);
-        const int q0 = (i_begin + it) * BM;
+        const int q0 = q_block(it) * BM, bq = q_head(it);
 #pragma unroll
         for (int p = 0; p < D / 64; ++p) {
-          tma_load_3d(sQ(s) + p * L::kQPanel, &tm_q, bar(L::kQFull + s), 64 * p, q0, bh);
-          tma_load_3d(sDO(s) + p * L::kQPanel, &tm_do, bar(L::kQFull + s), 64 * p, q0, bh);
+          tma_load_3d(sQ(s) + p * L::kQPanel, &tm_q, bar(L::kQFull + s), 64 * p, q0, bq);
+          tma_load_3d(sDO(s) + p * L::kQPanel, &tm_do, bar(L::kQFull + s), 64 * p, q0, bq);
         }
       }
     }
@@ -313,14 +324,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float c = args.scale_log2;
     float* sL = reinterpret_cast<float*>(smem + L::kLD);  // [2][2][BM]: (L*log2e, D) per buffer
-    const size_t row_base = (size_t)bh * N;
     // L and D of query column (block it, column cbeg + r) are fetched one block
     // ahead, so the global-memory latency overlaps the previous block's work.
     float pf_l = 0.f, pf_d = 0.f;
     bool pf_in = false;
     auto prefetch = [&](int it) {
-      const int q = (i_begin + it) * BM + cbeg + r;
-      pf_in = (r < kCW) && (it < nit) && (q < N);
+      if (it >= nit) {
+        pf_in = false;
+        return;
+      }
+      const int q = q_block(it) * BM + cbeg + r;
+      const size_t row_base = (size_t)q_head(it) * N;
+      pf_in = (r < kCW) && (q < N);
       if (pf_in) {
         pf_l = __ldg(args.lse + row_base + q);
         pf_d = __ldg(args.delta + row_base + q);
@@ -328,16 +343,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     prefetch(0);
     for (int it = 0; it < nit; ++it) {
-      const int q0 = (i_begin + it) * BM;
+      const int q0 = q_block(it) * BM;
       float* bufL = sL + (it & 1) * 2 * BM;
       float* bufD = bufL + BM;
       if (r < kCW) {
-        bufL[cbeg + r] = pf_in ? pf_l * kLog2e : INFINITY;  // rows past N get P = 0
+        // Rows past N get P = 0 through L = +inf; rows that see no key (L = -inf)
+        // get P = 0 through the causal mask below.
+        bufL[cbeg + r] = pf_in ? pf_l * kLog2e : INFINITY;
         bufD[cbeg + r] = pf_in ? pf_d : 0.f;
       }
       prefetch(it + 1);
       named_bar_sync(1 + e, 128);
-      const bool diag = args.causal && (key0 + kBN - 1 > q0);  // some key of the block is after some query
+      const bool diag = args.causal && (key0 + kBN - 1 > q0 + koff);  // some key is hidden from some query
       const int pb = it % NPB;
       // P^T of block it-NPB (TMEM buffer pb) and dS^T (smem buffer pb) are free once
       // that block's gradients are done.
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int u = 0; u < 4; ++u) {
             const int x = 4 * e4 + u;
             float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lv[u]));
-            if (diag && key > q0 + col + u) pe = 0.f;
+            if (diag && key > q0 + col + u + koff) pe = 0.f;
             p[32 * ch + x] = pe;
           }
         }
@@ -418,10 +435,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int wq = warp - 8;
     const int r = (wq << 5) + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    float* dq_acc = args.dq_acc + (size_t)bh * N * D;
     bool ok = true;
     for (int it = 0; it < nit; ++it) {
-      const int q0 = (i_begin + it) * BM;
+      const int q0 = q_block(it) * BM;
+      float* dq_acc = args.dq_acc + (size_t)q_head(it) * N * D;
       ok = mbar_wait(bar(L::kGrads + it % NPB), (it / NPB) & 1, args.err, kErrTimeoutMma);
       if (!ok) break;
       tc_fence_after();
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       // Final gradients of this key block; lane r holds key row key0 + r.
       const int key = key0 + r;
-      const size_t out_row = ((size_t)bh * N + key) * D + half * DH;
+      const size_t out_row = ((size_t)bh_kv * Nk + key) * D + half * DH;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col0 = which == 0 ? L::kColDV : L::kColDK;
@@ -496,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_32x32b_x32(tmem + lane_base + col0 + 32 * ch, v);
           tmem_wait_ld();
           reg_fence32(v);
-          if (key < N) {
+          if (key < Nk) {
 #pragma unroll
             for (int x = 0; x < 32; x += 8)
               st_global_v4(dst + 32 * ch + x,
@@ -589,8 +606,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
     auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, DQB, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
     if (e != cudaSuccess) return e;
-    const long long nkb = (a.N + kBN - 1) / kBN;
-    const long long grid = nkb * a.BH * (D / DH);
+    const long long nkb = (a.Nk + kBN - 1) / kBN;
+    const long long grid = nkb * a.BHkv * (D / DH);
     profile_mark_begin(stream);
     kern<<<(unsigned)grid, kBwdThreads, L::kAlloc, stream>>>(q, k, v, dout, a);
     e = cudaGetLastError();

@@ -95,20 +95,20 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
   // blocks see the most keys), so the last wave holds the lightest work.
   const int qb = args.num_qblocks - 1 - (int)(blockIdx.x / args.BH);
   const int bh = (int)(blockIdx.x % args.BH);
+  // Key/value head of this query head (grouped-query attention).
+  const int bh_kv = (bh / args.H) * (args.H / args.group) + (bh % args.H) / args.group;
   const int row0 = qb * (kBM * NQ);
+  const int Nk = args.Nk;
+  const int koff = Nk - N;  // causal mask: key j visible to query i iff j <= i + koff
 
-  // Key blocks each sub-tile visits (0 for a sub-tile entirely past the end).
+  // Key blocks each sub-tile visits (0 for a sub-tile past the end or with no visible key).
   int nblk[NQ];
   int nb = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) {
     const int r0 = row0 + kBM * t;
-    if (r0 >= N) {
-      nblk[t] = 0;
-    } else {
-      const int last_key = args.causal ? min(r0 + kBM - 1, N - 1) : N - 1;
-      nblk[t] = last_key / kBN + 1;
-    }
+    const int last_key = args.causal ? min(r0 + kBM - 1 + koff, Nk - 1) : Nk - 1;
+    nblk[t] = (r0 >= N || last_key < 0) ? 0 : last_key / kBN + 1;
     nb = max(nb, nblk[t]);
   }
 
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
         const CUtensorMap* m = (e & 1) ? &tm_v : &tm_k;
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * (e >> 1), bh);
+          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * (e >> 1), bh_kv);
       }
     }
   } else if (warp == kWarpMma) {
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       auto wait_full = [&](int e) -> bool {
         return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
       };
-      bool ok = mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
+      bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     const uint32_t tS = tmem + lane_base + L::s_col(t);
     const uint32_t tO = tmem + lane_base + L::o_col(t);
     const float c = args.scale_log2;
-    const int key_limit = args.causal ? min(q_row, N - 1) : N - 1;  // last key this row sees
+    const int key_limit = args.causal ? min(q_row + koff, Nk - 1) : Nk - 1;  // last key this row sees
     float m = -INFINITY;  // reference maximum (raw score units)
     float l = 0.f;        // running sum of 2^((s - m) c)
     bool ok = true;
@@ -316,8 +316,12 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       mbar_arrive(bar(L::kPFull + t));
       m = m_use;
     }
-    if (ok && my_blocks > 0) {
-      ok = mbar_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma);
+    const bool has_rows = row0 + kBM * t < N;
+    if (ok && has_rows) {
+      // A sub-tile whose rows see no key at all writes O = 0 and L = -inf; it still
+      // waits for its Q tile to land before reusing that shared memory.
+      ok = my_blocks > 0 ? mbar_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma)
+                         : mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -328,9 +332,14 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + 32 * ch, o);
-          tmem_wait_ld();
-          reg_fence32(o);
+          if (my_blocks > 0) {
+            tmem_ld_32x32b_x32(tO + 32 * ch, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int chunk = ch * 4 + k4;  // 16-byte chunk index along the row
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     }
     // All 128 threads of this sub-tile reach the barrier (ok or not), then one stores.
     named_bar_sync(1 + t, kBM);
-    if (ok && my_blocks > 0 && r == 0) {
+    if (ok && has_rows && r == 0) {
 #pragma unroll
       for (int p = 0; p < L::kPanels; ++p) tma_store_3d(&tm_o, sQ(t) + p * kPanelBytes, 64 * p, row0 + kBM * t, bh);
       tma_store_commit();

@@ -10,12 +10,15 @@ namespace fa {
 // Arguments of the forward kernel that are not TMA descriptors.
 struct FwdArgs {
   float* lse;            // [B*H, N] fp32 logsumexp output
-  int N;                 // sequence length
-  int BH;                // batch * heads
+  int N;                 // query rows per head (N_q)
+  int Nk;                // key/value rows per head (N_k)
+  int BH;                // batch * query heads
+  int H;                 // query heads per batch entry
+  int group;             // query heads per key/value head (H / H_kv)
   int num_qblocks;       // ceil(N / rows per CTA)
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e): scores go to base 2 with one multiply
-  int causal;            // key j hidden from query i when j > i
+  int causal;            // key j hidden from query i when j > i + (Nk - N)
   uint32_t* err;         // device error word
 };
 
@@ -28,10 +31,14 @@ struct BwdArgs {
   float* delta;          // [B*H, N] fp32 D = rowsum(dO o O) (workspace)
   void* dq;              // [B*H, N, d] 16-bit dQ output
   void* dk;              // [B*H, N, d] 16-bit dK output
-  void* dv;              // [B*H, N, d] 16-bit dV output
-  int N;
+  void* dv;              // [B*H_kv, Nk, d] 16-bit dV output (dk likewise)
+  int N;                 // query rows per head (N_q)
+  int Nk;                // key/value rows per head (N_k)
   int d;
-  int BH;
+  int BH;                // batch * query heads
+  int BHkv;              // batch * key/value heads
+  int H;                 // query heads per batch entry
+  int group;             // query heads per key/value head
   float scale;
   float scale_log2;
   int causal;

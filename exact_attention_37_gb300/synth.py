@@ -32,6 +32,16 @@ class Workload:
     value_scale: float = 1.0  # multiplies Q, K, V after the N(0,1) draw
     seeds: tuple = (0, 1, 2, 3)  # Q, K, V, dO
     backward: bool = True
+    H_kv: int | None = None  # key/value heads (grouped-query attention); None means H
+    N_k: int | None = None   # key/value rows; None means N
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.H_kv is None else self.H_kv
+
+    @property
+    def kv_len(self) -> int:
+        return self.N if self.N_k is None else self.N_k
 
     @property
     def scale(self) -> float:
@@ -63,14 +73,16 @@ def draw(shape, seed: int, dtype: str, value_scale: float = 1.0) -> torch.Tensor
 
 
 def make_inputs(w: Workload, with_dout: bool | None = None):
-    """Return CPU tensors ``(q, k, v, dout)`` in the storage type, layout [B, H, N, d].
+    """Return CPU tensors ``(q, k, v, dout)`` in the storage type: q and dout
+    [B, H, N, d], k and v [B, H_kv, N_k, d].
 
     ``dout`` is drawn unscaled (N(0,1)); it is ``None`` when not requested.
     """
     shape = (w.B, w.H, w.N, w.d)
+    kv_shape = (w.B, w.kv_heads, w.kv_len, w.d)
     q = draw(shape, w.seeds[0], w.dtype, w.value_scale)
-    k = draw(shape, w.seeds[1], w.dtype, w.value_scale)
-    v = draw(shape, w.seeds[2], w.dtype, w.value_scale)
+    k = draw(kv_shape, w.seeds[1], w.dtype, w.value_scale)
+    v = draw(kv_shape, w.seeds[2], w.dtype, w.value_scale)
     want = w.backward if with_dout is None else with_dout
     do = draw(shape, w.seeds[3], w.dtype, 1.0) if want else None
     return q, k, v, do

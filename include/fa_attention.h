@@ -76,6 +76,21 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * Forward pass with grouped-query attention and unequal lengths.
+ *   q, o : [B, H, N_q, d];  k, v : [B, H_kv, N_k, d];  lse : [B, H, N_q] fp32.
+ *   H_kv >= 1 divides H; query head h reads key/value head h / (H / H_kv)
+ *   (H_kv = 1 is multi-query attention; MQA support is named on the page
+ *   "FlashAttention — فلاش أتنشن", section "FlashAttention-2").
+ *   Under causal != 0 the mask is aligned at the bottom right: key j is visible
+ *   to query i iff j <= i + (N_k - N_q), so the last query row sees every key.
+ *   A query row that sees no key (only when N_q > N_k) gets O = 0, L = -inf.
+ *   N_k must be >= 1 when B*H*N_q > 0 (FA_ERR_UNSUPPORTED otherwise).
+ * fa_fwd(..., N, ...) is fa_fwd_ex with H_kv = H and N_q = N_k = N.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                    int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Bytes of device workspace `fa_bwd` needs: an fp32 dQ accumulator [B,H,N,d],
  * the fp32 row vector D [B,H,N], and alignment padding.  Linear in N.
  * Returns 0 for invalid or empty sizes.
@@ -102,6 +117,19 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                  float scale, int causal, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Backward pass with grouped-query attention and unequal lengths; shapes as in
+ * fa_fwd_ex (dq like q, dk and dv like k).  The gradient of a shared key/value
+ * head is the sum over the query heads of its group (computed inside one CTA
+ * per key block, without atomics on dK/dV).  The workspace is
+ * fa_bwd_workspace_size(B, H, N_q, d) bytes.  With B*H*N_q == 0 no query
+ * row exists, so dk and dv are set to zero (cudaMemsetAsync on `stream`).
+ * fa_bwd(..., N, ...) is fa_bwd_ex with H_kv = H and N_q = N_k = N.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                    int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
  * fa_bwd without a caller-provided workspace, for callers that cannot allocate

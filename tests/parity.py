@@ -44,6 +44,10 @@ def compare_o(w, got, ref, what="O"):
 
 
 def compare_l(got, ref):
+    # rows that see no key have L = -inf on both sides
+    inf = np.isinf(ref)
+    assert np.array_equal(np.isinf(got), inf) and np.all(got[inf] == ref[inf]), "L: infinite rows differ"
+    got, ref = got[~inf], ref[~inf]
     err = float(np.abs(got - ref).max()) if got.size else 0.0
     assert err <= L_ABS, f"L: max abs err {err:.3e} > {L_ABS}"
     return err

@@ -65,6 +65,21 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib, over, code):
     assert fwd(lib, **over) == code
 
 
+def test_grouped_and_unequal_lengths_validation(lib):
+    vp = ctypes.c_void_p
+    p = [vp(16)] * 5
+
+    def ex(B=1, H=4, Hkv=2, Nq=8, Nk=8, d=64):
+        return lib.fa_fwd_ex(*p, B, H, Hkv, Nq, Nk, d, 0.125, 1, 1, None)
+
+    assert ex(Hkv=3) == 1      # H_kv must divide H
+    assert ex(Hkv=0) == 1
+    assert ex(Nk=-1) == 1
+    assert ex(Nk=0) == 2       # queries with an empty key set
+    assert ex(Nq=0) == 0       # no query rows: nothing to do
+    assert ex(d=80) == 2
+
+
 def test_fwd_empty_problem_is_a_no_op(lib):
     assert fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0
     assert fwd(lib, B=0) == 0
