@@ -51,7 +51,7 @@ def forward(q, k, v, scale: float | None = None, causal: bool = False, stream=No
 
 
 def backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, stream=None, workspace=None):
-    """Returns (dQ, dK, dV) like q.  ``workspace`` (uint8 CUDA tensor) is allocated if not given."""
+    """Returns (dQ, dK, dV) like q, k, v.  ``workspace`` (uint8 CUDA tensor) is allocated if not given."""
     import torch
 
     B, H, N, d = q.shape

@@ -37,6 +37,7 @@ SIGNATURES = {
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_check_device_status": (_i, [_vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
+    "fa_last_device_error_detail": (None, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_profile_begin": (_i, [_i]),
     "fa_profile_end": (_i, [_vp, _vp, _i]),
@@ -45,8 +46,9 @@ SIGNATURES = {
 
 
 class FaError(RuntimeError):
-    def __init__(self, where: str, code: int):
-        super().__init__(f"{where} failed: {STATUS.get(code, code)}")
+    def __init__(self, where: str, code: int, detail=None):
+        extra = f" (device record {detail})" if detail else ""
+        super().__init__(f"{where} failed: {STATUS.get(code, code)}{extra}")
         self.code = code
 
 
@@ -159,7 +161,12 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool
 
 def fa_check_device_status(stream=None):
     """Synchronize and raise FaError(FA_ERR_DEVICE_TIMEOUT) if a kernel gave up on a wait."""
-    _check("fa_check_device_status", load().fa_check_device_status(_stream(stream)))
+    lib = load()
+    code = lib.fa_check_device_status(_stream(stream))
+    if code != FA_OK:
+        rec = (ctypes.c_uint32 * 4)()
+        lib.fa_last_device_error_detail(rec)
+        raise FaError("fa_check_device_status", code, [hex(x) for x in rec])
 
 
 def fa_profile_begin(n: int):
@@ -174,7 +181,8 @@ def fa_profile_end(max_out: int = 65536):
     n = load().fa_profile_end(ms, kind, max_out)
     if n < 0:
         raise FaError("fa_profile_end", 5)
-    return [("fwd" if kind[i] == 0 else "bwd", float(ms[i])) for i in range(n)]
+    names = {0: "fwd", 1: "bwd"}
+    return [(names.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n)]
 
 
 def fa_status_string(code: int) -> str:

@@ -17,13 +17,14 @@
 
 namespace fa {
 
-// Device word the kernels set when a bounded wait gives up (one per device that loads the library).
-__device__ uint32_t g_error_word;
+// Device error record the kernels write when a bounded wait gives up (one per
+// device that loads the library): bits, first failure code, its CTA, its barrier.
+__device__ uint32_t g_error_word[4];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-uint32_t g_last_bits = 0;
+uint32_t g_last_detail[4] = {0, 0, 0, 0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -305,18 +306,23 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 
 fa_status fa_check_device_status(fa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
-  uint32_t bits = 0;
-  if (cudaMemcpyFromSymbol(&bits, g_error_word, sizeof(bits)) != cudaSuccess) return FA_ERR_CUDA;
-  g_last_bits = bits;
-  if (bits != 0) {
-    const uint32_t zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t rec[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(rec, g_error_word, sizeof(rec)) != cudaSuccess) return FA_ERR_CUDA;
+  for (int i = 0; i < 4; ++i) g_last_detail[i] = rec[i];
+  if (rec[0] != 0) {
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_error_word, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
     return FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;
 }
 
-uint32_t fa_last_device_error_bits(void) { return g_last_bits; }
+uint32_t fa_last_device_error_bits(void) { return g_last_detail[0]; }
+
+void fa_last_device_error_detail(uint32_t* out4) {
+  if (!out4) return;
+  for (int i = 0; i < 4; ++i) out4[i] = g_last_detail[i];
+}
 
 const char* fa_status_string(fa_status s) {
   switch (s) {

@@ -82,7 +82,9 @@ struct BwdLayout {
   static constexpr int kGrads = kDsFull + 2;                      // one per P^T/dS^T buffer
   static constexpr int kDqFree = kGrads + NPB;
   static constexpr int kDrain = kDqFree + 1;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kEwSync = kDrain + 1;                      // two: one per elementwise warpgroup
+  static constexpr int kWqSync = kEwSync + 2;                     // the dQ warpgroup
+  static constexpr int kNumBars = kWqSync + 1;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -177,6 +179,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int b = 0; b < NPB; ++b) mbar_init(bar(L::kGrads + b), 1);
     mbar_init(bar(L::kDqFree), 128);
     mbar_init(bar(L::kDrain), 1);
+    mbar_init(bar(L::kEwSync + 0), 128);
+    mbar_init(bar(L::kEwSync + 1), 128);
+    mbar_init(bar(L::kWqSync), 128);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (STG == 1 && it + 1 < nit && !(ok = next_scores(it))) break;
       }
       mma_commit(bar(L::kDrain));
-      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
+      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma, false);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ P^T and dS^T
@@ -342,6 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     };
     prefetch(0);
+    SmemSync wg_sync{bar(L::kEwSync + e), 0u};
     for (int it = 0; it < nit; ++it) {
       const int q0 = q_block(it) * BM;
       float* bufL = sL + (it & 1) * 2 * BM;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bufD[cbeg + r] = pf_in ? pf_d : 0.f;
       }
       prefetch(it + 1);
-      named_bar_sync(1 + e, 128);
+      if (!wg_sync.sync(args.err)) break;
       const bool diag = args.causal && (key0 + kBN - 1 > q0 + koff);  // some key is hidden from some query
       const int pb = it % NPB;
       // P^T of block it-NPB (TMEM buffer pb) and dS^T (smem buffer pb) are free once
@@ -436,6 +442,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = (wq << 5) + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     bool ok = true;
+    SmemSync wq_sync{bar(L::kWqSync), 0u};
     for (int it = 0; it < nit; ++it) {
       const int q0 = q_block(it) * BM;
       float* dq_acc = args.dq_acc + (size_t)q_head(it) * N * D;
@@ -457,12 +464,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // and the accumulation uses 128-bit reductions (a quarter of the
         // instructions of per-column ones).
         const uint32_t stg = sbase + L::kDqStage;
-        named_bar_sync(3, 128);  // the previous block's staged rows have been read
+        if (!(ok = wq_sync.sync(args.err))) break;  // the previous block's staged rows have been read
 #pragma unroll
         for (int ch = 0; ch < kCh; ++ch)
 #pragma unroll
           for (int x = 0; x < 32; ++x) st_shared_f32(stg + (32 * ch + x) * L::kDqRowBytes + 4 * r, v[ch][x]);
-        named_bar_sync(3, 128);
+        if (!(ok = wq_sync.sync(args.err))) break;
         constexpr int kV4PerRow = DH / 4;
 #pragma unroll 4
         for (int j = r; j < BM * kV4PerRow; j += 128) {
@@ -566,9 +573,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, lon
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) args.delta[row] = acc;
-    float* z = args.dq_acc + base;
+    if (args.dq_acc) {
+      float* z = args.dq_acc + base;
 #pragma unroll
-    for (int e = 0; e < kPer; e += 2) *reinterpret_cast<float2*>(z + e) = make_float2(0.f, 0.f);
+      for (int e = 0; e < kPer; e += 2) *reinterpret_cast<float2*>(z + e) = make_float2(0.f, 0.f);
+    }
   }
 }
 

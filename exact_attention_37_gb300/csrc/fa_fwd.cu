@@ -222,7 +222,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       }
       // Every MMA must have finished before TMEM can be released.
       mma_commit(bar(L::kDrain));
-      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
+      mbar_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma, false);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue

@@ -16,12 +16,16 @@ namespace fa {
 enum : uint32_t {
   kErrTimeoutTma = 1u << 0,       // a consumer waited too long for a TMA tile
   kErrTimeoutMma = 1u << 1,       // a waiter never saw a tensor-core commit
-  kErrTimeoutSoftmax = 1u << 2,   // the MMA issuer never saw softmax output
+  kErrTimeoutSoftmax = 1u << 2,   // the MMA issuer never saw elementwise output
   kErrTimeoutRing = 1u << 3,      // the producer never got a free ring slot
+  kErrTimeoutSync = 1u << 4,      // a warpgroup barrier never completed
+  kErrAborted = 1u << 31,         // set with the first failure: every later wait gives up at once
 };
 
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of wall clock per wait
+// Device error record: [0] the bits above; [1] the code of the first failure;
+// [2] its CTA index; [3] its barrier's shared-memory offset.
 
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of wall clock per wait
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -57,18 +61,51 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
   return ok;
 }
 // Wait for the phase with the given parity to complete.  Returns false (after
-// setting `code` in *err) if it did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
+// recording `code` in the error record err[0..3]) if it did not complete within
+// kWaitLimitNs, or at once if another wait of any CTA has already given up (the
+// abort bit), so a failure ends the kernel quickly instead of hanging it.
+// Records a wait that gave up: the first failure's code, CTA and barrier, then
+// the abort bit that makes every other wait of the grid give up at once.  Out of
+// line: it runs at most once per thread and keeps the hot wait loops small.
+static __device__ __noinline__ void record_timeout(uint32_t* err, uint32_t code, uint32_t bar) {
+  if (!err) return;
+  if (atomicCAS(err + 1, 0u, code) == 0u) {
+    err[2] = blockIdx.x;
+    err[3] = bar;
+  }
+  atomicOr(err, code | kErrAborted);
+}
+
+// The final drain of a CTA's tensor-core work passes honor_abort = false: it
+// always waits (bounded) for the MMAs already issued before TMEM is released.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                          bool honor_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      if (err) atomicOr(err, code);
-      return false;
+    if ((n & 63) == 63) {
+      if (honor_abort && (*reinterpret_cast<volatile uint32_t*>(err) & kErrAborted)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        record_timeout(err, code, bar);
+        return false;
+      }
     }
   }
 }
+
+// A barrier among `count` threads built on an mbarrier, so that its wait is
+// bounded like every other wait: each thread arrives, then waits for the phase.
+struct SmemSync {
+  uint32_t bar;
+  uint32_t phase;
+  __device__ __forceinline__ bool sync(uint32_t* err) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, err, kErrTimeoutSync);
+    phase ^= 1u;
+    return ok;
+  }
+};
 
 // ---------------------------------------------------------------- proxies / barriers
 __device__ __forceinline__ void fence_proxy_async_smem() {

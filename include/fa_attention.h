@@ -125,6 +125,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * per key block, without atomics on dK/dV).  The workspace is
  * fa_bwd_workspace_size(B, H, N_q, d) bytes.  With B*H*N_q == 0 no query
  * row exists, so dk and dv are set to zero (cudaMemsetAsync on `stream`).
+ * dK and dV are deterministic (one CTA sums each key row in a fixed order);
+ * dQ accumulates fp32 reductions from every key block, so its last bits depend
+ * on scheduling.
  * fa_bwd(..., N, ...) is fa_bwd_ex with H_kv = H and N_q = N_k = N.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -169,6 +172,16 @@ fa_status fa_check_device_status(fa_stream_t stream);
 
 /* Raw device error word of the last fa_check_device_status (0 = none). */
 uint32_t fa_last_device_error_bits(void);
+
+/*
+ * The error record behind it: out4[0] the bits, out4[1] the code of the first
+ * wait that gave up (1 TMA tile, 2 tensor-core commit, 4 elementwise output,
+ * 8 ring slot, 16 warpgroup barrier), out4[2] that CTA's index, out4[3] its
+ * barrier's shared-memory address.  After the first failure every other wait
+ * of the grid gives up at once (bit 31), and kernels launched before the next
+ * fa_check_device_status stop early: their results are not valid.
+ */
+void fa_last_device_error_detail(uint32_t* out4);
 
 /*
  * Measurement hook.  fa_profile_begin(n) makes the next n calls of fa_fwd and
