@@ -48,11 +48,25 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def profile_traffic(kernel_tag):
-    """DRAM bytes per launch of a kernel from its committed ncu summary, if the kernel
-    source has not changed since the capture (else None)."""
+def sources_sha256(paths):
+    """sha256 over the listed files' bytes, in order (paths relative to the repo root)."""
     import hashlib
 
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(HERE, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profile_traffic(kernel_tag):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if none of the
+    sources the kernel was built from has changed since the capture (else None).
+
+    The summary lists ``- source: `a`, `b` ...`` (comma-separated, repo-relative),
+    ``- source_sha256: `...` `` (over those files in order) and
+    ``- traffic_bytes_per_launch: `...` ``.
+    """
     summ = os.path.join(HERE, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(summ):
         return None
@@ -60,14 +74,13 @@ def profile_traffic(kernel_tag):
     for line in open(summ):
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    src = fields.get("source")
-    want = fields.get("source_sha256")
-    tb = fields.get("traffic_bytes_per_launch")
-    if not (src and want and tb):
+            fields[k.strip()] = v.strip()
+    srcs = [x.strip().strip("`") for x in fields.get("source", "").split(",") if x.strip()]
+    want = fields.get("source_sha256", "").strip("`")
+    tb = fields.get("traffic_bytes_per_launch", "").strip("`")
+    if not (srcs and want and tb):
         return None
-    path = os.path.join(HERE, src)
-    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != want:
+    if not all(os.path.exists(os.path.join(HERE, x)) for x in srcs) or sources_sha256(srcs) != want:
         return None
     try:
         return float(tb)
@@ -160,44 +173,92 @@ def reduce_max(x, world, device):
     return float(t.item())
 
 
-def cpu_oracle_sample(w, heads=1):
-    """Time the oracle (as it stands) on `heads` heads of the workload, forward + backward."""
+def visible_pairs(w, rows):
+    """(query, key) pairs the mask leaves visible in the given query rows of one head."""
+    import numpy as np
+
+    rows = np.asarray(rows, dtype=np.int64)
+    if not w.causal:
+        return int(rows.size) * w.kv_len
+    return int(np.clip(rows + (w.kv_len - w.N) + 1, 0, w.kv_len).sum())
+
+
+def oracle_rows(w, q, k, v, do, bh, rows, backward, chunk=1024):
+    """Run the oracle (as it stands) on some query rows of one head, `chunk` rows at a time;
+    returns the algorithmic FLOPs of those rows (4d per visible pair forward, 10d backward)."""
     import numpy as np
 
     import oracle
+
+    b, h = divmod(bh, w.H)
+    g = h // (w.H // w.kv_heads)
+    for r0 in range(0, len(rows), chunk):
+        rr = np.asarray(rows[r0:r0 + chunk])
+        oracle.forward_rows(q[b, h], k[b, g], v[b, g], w.scale, w.causal, rr)
+        if backward:
+            oracle.head_backward_rows(q[b, h], k[b, g], v[b, g], do[b, h], w.scale, w.causal, rr)
+    return visible_pairs(w, rows) * w.d * (14 if backward else 4)
+
+
+def cpu_oracle_sample(w, q, k, v, do, backward=True, min_seconds=10.0):
+    """Time the oracle on whole heads of the workload, head after head, until at least
+    `min_seconds` of CPU work; returns (TFLOP/s, seconds, heads)."""
+    import numpy as np
+
+    rows = np.arange(w.N)
+    flops, heads = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        flops += oracle_rows(w, q, k, v, do, heads % (w.B * w.H), rows, backward)
+        heads += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            return flops / dt / 1e12, dt, heads
+
+
+def run_reference(args, w, backward):
+    """The reference arm: the fp64 oracle as it stands, on the host cores.  Each step is a
+    strided sample of query rows of one head (forward, and backward if the workload has
+    one), sized so that warm-up plus timed steps take about two minutes in all."""
+    import numpy as np
+
     from exact_attention_37_gb300.synth import make_inputs
 
-    q, k, v, do = make_inputs(w.with_(B=1, H=heads), with_dout=True)
-    t0 = time.perf_counter()
-    for h in range(heads):
-        oracle.forward_rows(q[0, h], k[0, h], v[0, h], w.scale, w.causal, np.arange(w.N))
-        oracle.head_backward_rowwise(q[0, h], k[0, h], v[0, h], do[0, h], w.scale, w.causal)
-    dt = time.perf_counter() - t0
-    flops = attention_flops(w.with_(B=1, H=heads))
-    return flops / dt / 1e12, dt
-
-
-def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    cores = os.cpu_count()
-    for _ in range(args.warmup):
-        cpu_oracle_sample(w, 1)
-    vals, secs = [], []
-    for _ in range(args.steps):
-        v, dt = cpu_oracle_sample(w, 1)
-        vals.append(v)
+    q, k, v, do = make_inputs(w.with_(B=1, H=min(w.H, 4), H_kv=None if w.H_kv is None else 1), with_dout=True)
+    ws = w.with_(B=1, H=q.shape[1], H_kv=None if w.H_kv is None else 1)
+    budget = 120.0 / (args.steps + args.warmup)
+    t0 = time.perf_counter()
+    oracle_rows(ws, q, k, v, do, 0, np.arange(0, w.N, max(1, w.N // 64)), backward)
+    per_row = (time.perf_counter() - t0) / len(range(0, w.N, max(1, w.N // 64)))
+    R = int(min(w.N, max(8, budget / max(per_row, 1e-9))))
+    spread = max(1, w.N // R)
+
+    def one(i):
+        rows = np.unique((i % spread + (np.arange(R) * w.N) // R) % w.N)
+        t = time.perf_counter()
+        f = oracle_rows(ws, q, k, v, do, i % (ws.B * ws.H), rows, backward)
+        return f, time.perf_counter() - t
+
+    for i in range(args.warmup):
+        one(i)
+    flops, secs = 0, []
+    for i in range(args.steps):
+        f, dt = one(args.warmup + i)
+        flops += f
         secs.append(dt)
-    value = statistics.mean(vals)
-    sample = f"1 of {w.B * w.H} heads per step, forward + backward, fp64 numpy (row chunks of 1024)"
+    value = flops / sum(secs) / 1e12
+    sample = (f"{R} evenly spaced query rows of one head per step, forward"
+              f"{' + backward' if backward else ''}, fp64 numpy; FLOPs of the rows' visible pairs")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                   "input_dtype": w.dtype},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+                   "input_dtype": w.dtype, "step": "fwd + bwd" if backward else "fwd"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -210,6 +271,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_B2_H16_N8192_d128_bf16_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--causal", type=int, choices=[0, 1], default=None, help="override the workload's mask")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward pass alone (default for forward-only workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -217,8 +280,14 @@ def main():
     from exact_attention_37_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
+    profile_key = w.name.split("_")[0]
+    if args.causal is not None and bool(args.causal) != w.causal:
+        base = w.name[: -len("_causal")] if w.name.endswith("_causal") else w.name
+        w = w.with_(causal=bool(args.causal), name=base + ("_causal" if args.causal else ""))
+        profile_key += "_causal" if args.causal else "_full"
+    fwd_only = args.fwd_only or not w.backward
     if args.impl == "reference":
-        run_reference(args, w)
+        run_reference(args, w, backward=not fwd_only)
         return
 
     import torch
@@ -237,14 +306,21 @@ def main():
     B, H, N, d = qd.shape
     od = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    if fwd_only:
+        dq = dk = dv = ws = None
+    else:
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def run_bwd():
+        if not fwd_only:
+            fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
+
     def step():
         fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
-        fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
+        run_bwd()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -263,7 +339,7 @@ def main():
             e0.record(stream)
             fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
             e1.record(stream)
-            fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, ws, w.scale, w.causal)
+            run_bwd()
             e2.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -277,27 +353,32 @@ def main():
     total_ms = reduce_max(sum(step_ms), world, dev)
     ms_per_step = total_ms / K
 
-    flops_step = attention_flops(w)
     flops_fwd = attention_flops(w, backward=False)
+    flops_step = flops_fwd if fwd_only else attention_flops(w)
     value = world * flops_step * K / (total_ms / 1e3) / 1e12
 
     # ---- end to end through the C ABI with host buffers
     pin = lambda t: t.pin_memory()
     qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
-    oh, dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v, q))
+    oh = torch.empty_like(q).pin_memory()
     lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh, doh))
-    d2h = sum(x.numel() * x.element_size() for x in (oh, lseh, dqh, dkh, dvh))
+    uploads = [(qh, qd), (kh, kd), (vh, vd)] + ([] if fwd_only else [(doh, dod)])
+    downloads = [(od, oh), (lse, lseh)]
+    if not fwd_only:
+        dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v))
+        downloads += [(dq, dqh), (dk, dkh), (dv, dvh)]
+    h2d = sum(hx.numel() * hx.element_size() for hx, _ in uploads)
+    d2h = sum(hx.numel() * hx.element_size() for _, hx in downloads)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     barrier(world)
     for i in range(K):
         flush.zero_()
         e2e_ev[i][0].record(stream)
-        for hsrc, dst in ((qh, qd), (kh, kd), (vh, vd), (doh, dod)):
+        for hsrc, dst in uploads:
             dst.copy_(hsrc, non_blocking=True)
         step()
-        for dsrc, hdst in ((od, oh), (lse, lseh), (dq, dqh), (dk, dkh), (dv, dvh)):
+        for dsrc, hdst in downloads:
             hdst.copy_(dsrc, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -309,12 +390,13 @@ def main():
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
     fwd_avg = statistics.mean(fwd_kernel_ms)
-    bwd_main_avg = statistics.mean(bwd_main_ms)
-    flops_bwd = flops_step - flops_fwd
+    bwd_main_avg = statistics.mean(bwd_main_ms) if bwd_main_ms else 0.0
+    flops_bwd = attention_flops(w) - flops_fwd
     if bwd_main_avg >= fwd_avg:
-        dom, dom_ms, dom_flops, tag = "fa_bwd_kernel", bwd_main_avg, flops_bwd, "fa_bwd_kernel_long"
+        dom, dom_ms, dom_flops = "fa_bwd_kernel", bwd_main_avg, flops_bwd
     else:
-        dom, dom_ms, dom_flops, tag = "fa_fwd_kernel", fwd_avg, flops_fwd, "fa_fwd_kernel_long"
+        dom, dom_ms, dom_flops = "fa_fwd_kernel", fwd_avg, flops_fwd
+    tag = f"{dom}_{profile_key}"
     peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     fwd_tflops = flops_fwd / (fwd_avg / 1e3) / 1e12
@@ -324,10 +406,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        heads = 2
-        cv, cdt = cpu_oracle_sample(w, heads)
+        cv, cdt, heads = cpu_oracle_sample(w, q, k, v, do, backward=not fwd_only)
         cpu = {"value": cv, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{heads} of {w.B * w.H} heads, forward + backward, fp64 numpy, {cdt:.1f} s"}
+               "sample": f"{heads} head(s) of the {w.B * w.H}, forward{'' if fwd_only else ' + backward'}, "
+                         f"fp64 numpy, {cdt:.1f} s; FLOPs of the visible pairs"}
 
     if rank == 0:
         out = {
@@ -335,15 +417,17 @@ def main():
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-                       "step": "fwd + bwd (pre, main, dq convert)", "l2": "256 MB flush write before every step",
-                       "parallelism": f"replicas x{world}"},
+                       "step": "fwd" if fwd_only else "fwd + bwd (pre, main, dq convert)",
+                       "l2": "256 MB flush write before every step", "parallelism": f"replicas x{world}"},
             "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"])},
-            "bwd": {"tflops": flops_bwd / (statistics.mean(bwd_ms) / 1e3) / 1e12, "ms": statistics.mean(bwd_ms),
-                    "main_kernel_ms": bwd_main_avg},
+            "bwd": None if fwd_only else {
+                "tflops": flops_bwd / (statistics.mean(bwd_ms) / 1e3) / 1e12, "ms": statistics.mean(bwd_ms),
+                "main_kernel_ms": bwd_main_avg,
+                "main_kernel_frac_of_peak_sustained": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / peak},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 4 * K,
+            "gpu_launches": (1 if fwd_only else 4) * K,
             "clocks": clocks.summary(),
         }
         print(json.dumps(out))

@@ -7,6 +7,7 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_forward,
     forward_rows,
+    head_backward_rows,
     head_backward_rowwise,
     probabilities,
     scores,

@@ -54,6 +54,7 @@ __all__ = [
     "attention_forward",
     "attention_backward",
     "forward_rows",
+    "head_backward_rows",
     "head_backward_rowwise",
 ]
 
@@ -169,13 +170,31 @@ def forward_rows(q_h, k_h, v_h, scale: float, causal: bool, rows):
     return P @ v_h, L
 
 
+def head_backward_rows(q_h, k_h, v_h, do_h, scale: float, causal: bool, rows):
+    """One head's backward pass restricted to the query rows ``rows``.
+
+    Returns (dQ[rows], dK part, dV part, D[rows]): the rows' own dQ and D, and
+    their contributions to dK and dV (the full dK, dV are the sums of these parts
+    over any partition of the rows).  Every quantity comes from the definition
+    for those rows alone: P, then O = P V, dP = dO V^T, D, dS = P o (dP - D).
+    """
+    q_h, k_h, v_h, do_h = _f64(q_h), _f64(k_h), _f64(v_h), _f64(do_h)
+    rows = np.asarray(rows)
+    P, _ = probabilities(scores(q_h, k_h, scale, causal, rows=rows))
+    O = P @ v_h
+    dP = do_h[rows] @ v_h.T
+    Dr = (do_h[rows] * O).sum(axis=1)
+    dS = P * (dP - Dr[:, None])
+    return scale * (dS @ k_h), scale * (dS.T @ q_h[rows]), P.T @ do_h[rows], Dr
+
+
 def head_backward_rowwise(q_h, k_h, v_h, do_h, scale: float, causal: bool, chunk: int = 1024):
     """dQ, dK, dV, D of one head, evaluating the definition over chunks of query rows.
 
     For long sequences the N x N matrices of one head do not fit comfortably in
-    host memory, so rows are taken ``chunk`` at a time: every row's P, dP and dS
-    come from the definition for that row alone, dQ rows are written directly,
-    and the dK, dV sums over rows are accumulated chunk after chunk.
+    host memory, so rows are taken ``chunk`` at a time (``head_backward_rows``):
+    dQ rows are written directly and the dK, dV sums over rows are accumulated
+    chunk after chunk.
     """
     q_h, k_h, v_h, do_h = _f64(q_h), _f64(k_h), _f64(v_h), _f64(do_h)
     N, d = q_h.shape
@@ -185,13 +204,7 @@ def head_backward_rowwise(q_h, k_h, v_h, do_h, scale: float, causal: bool, chunk
     D = np.empty(N)
     for r0 in range(0, N, chunk):
         rows = np.arange(r0, min(N, r0 + chunk))
-        P, _ = probabilities(scores(q_h, k_h, scale, causal, rows=rows))
-        O = P @ v_h
-        dP = do_h[rows] @ v_h.T
-        Dr = (do_h[rows] * O).sum(axis=1)
-        dS = P * (dP - Dr[:, None])
-        dQ[rows] = scale * (dS @ k_h)
-        dK += scale * (dS.T @ q_h[rows])
-        dV += P.T @ do_h[rows]
-        D[rows] = Dr
+        dQ[rows], dk, dv, D[rows] = head_backward_rows(q_h, k_h, v_h, do_h, scale, causal, rows)
+        dK += dk
+        dV += dv
     return dQ, dK, dV, D

@@ -59,12 +59,17 @@ def test_profile_traffic_requires_matching_source(tmp_path, monkeypatch):
 
     src = tmp_path / "k.cu"
     src.write_text("kernel")
+    hdr = tmp_path / "k.cuh"
+    hdr.write_text("header")
     prof = tmp_path / "profiles"
     prof.mkdir()
-    h = hashlib.sha256(b"kernel").hexdigest()
-    (prof / "tag.md").write_text(f"- source: `k.cu`\n- source_sha256: `{h}`\n- traffic_bytes_per_launch: `1234`\n")
+    h = hashlib.sha256(b"kernelheader").hexdigest()
+    (prof / "tag.md").write_text(f"- source: `k.cu`, `k.cuh`\n- source_sha256: `{h}`\n- traffic_bytes_per_launch: `1234`\n")
     monkeypatch.setattr(bench, "HERE", str(tmp_path))
     assert bench.profile_traffic("tag") == 1234.0
+    hdr.write_text("changed header")
+    assert bench.profile_traffic("tag") is None
+    hdr.write_text("header")
     src.write_text("changed kernel")
     assert bench.profile_traffic("tag") is None
 

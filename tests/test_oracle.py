@@ -259,6 +259,23 @@ def test_rowwise_backward_matches_full(causal):
         assert np.abs(a[0, 0] - b).max() < 1e-12
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_subset_backward_parts_sum_to_the_full_gradients(causal):
+    # an uneven, out-of-order partition of the rows: dQ and D rows match, dK and dV parts add up
+    q, k, v, do = (rnd((1, 1, 19, 6), t) for t in (71, 72, 73, 74))
+    dQ, dK, dV, D = oracle.attention_backward(q, k, v, do, 0.7, causal)
+    parts = [[18, 3, 11], list(range(0, 3)), [4, 5, 6, 7, 8, 9, 10], [12, 13, 14, 15, 16, 17]]
+    sk, sv = np.zeros_like(dK[0, 0]), np.zeros_like(dV[0, 0])
+    for rows in parts:
+        dq, dk, dv, dr = oracle.head_backward_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.7, causal, rows)
+        assert np.abs(dq - dQ[0, 0, rows]).max() < 1e-12
+        assert np.abs(dr - D[0, 0, rows]).max() < 1e-12
+        sk += dk
+        sv += dv
+    assert np.abs(sk - dK[0, 0]).max() < 1e-12
+    assert np.abs(sv - dV[0, 0]).max() < 1e-12
+
+
 def test_accepts_16bit_tensors_exactly():
     x = torch.randn(1, 1, 4, 8).to(torch.bfloat16)
     assert np.array_equal(oa._f64(x), x.float().numpy().astype(np.float64))
