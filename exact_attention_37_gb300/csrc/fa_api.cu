@@ -147,6 +147,16 @@ void profile_mark_end(cudaStream_t stream, int kind) {
 
 int bwd_query_rows(int d);
 
+size_t bwd_lse_offset(long long BH, int N, int d) {
+  return bwd_needs_dq_acc(d) ? round_up((size_t)BH * N * d * sizeof(float), 256) : 0;
+}
+size_t bwd_delta_offset(long long BH, int N, int d) {
+  return bwd_lse_offset(BH, N, d) + round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256);
+}
+size_t bwd_workspace_bytes(long long BH, int N, int d) {
+  return bwd_delta_offset(BH, N, d) + round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256);
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -192,9 +202,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_common(B, H, H > 0 ? 1 : 0, N, N, d, 1.f, FA_FP16) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  if (rows == 0) return 0;
-  return round_up(rows * d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+  if ((size_t)B * H * N == 0) return 0;
+  return bwd_workspace_bytes((long long)B * H, N, d);
 }
 
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -227,13 +236,14 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   if (!make_map(&mq, q, BH, N_q, d, bf16, bm) || !make_map(&mk, k, BHkv, N_k, d, bf16, 128) ||
       !make_map(&mv, v, BHkv, N_k, d, bf16, 128) || !make_map(&mdo, dout, BH, N_q, d, bf16, bm))
     return FA_ERR_CUDA;
-  const size_t rows = (size_t)BH * N_q;
   BwdArgs a{};
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.dq_acc = static_cast<float*>(workspace);
-  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * d * sizeof(float), 256));
+  a.dq_acc = bwd_needs_dq_acc(d) ? static_cast<float*>(workspace) : nullptr;
+  a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_lse_offset(BH, N_q, d));
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_delta_offset(BH, N_q, d));
+  a.Npad = bwd_npad(N_q);
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

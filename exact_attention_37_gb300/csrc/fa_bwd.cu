@@ -339,10 +339,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         return;
       }
       const int q = q_block(it) * BM + cbeg + r;
-      const size_t row_base = (size_t)q_head(it) * N;
+      const size_t row_base = (size_t)q_head(it) * args.Npad;
       pf_in = (r < kCW) && (q < N);
       if (pf_in) {
-        pf_l = __ldg(args.lse + row_base + q);
+        pf_l = __ldg(args.lse_log2 + row_base + q);
         pf_d = __ldg(args.delta + row_base + q);
       }
     };
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (r < kCW) {
         // Rows past N get P = 0 through L = +inf; rows that see no key (L = -inf)
         // get P = 0 through the causal mask below.
-        bufL[cbeg + r] = pf_in ? pf_l * kLog2e : INFINITY;
+        bufL[cbeg + r] = pf_in ? pf_l : INFINITY;
         bufD[cbeg + r] = pf_in ? pf_d : 0.f;
       }
       prefetch(it + 1);
@@ -542,17 +542,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// D_i = sum_c dO_ic O_ic per row, and the fp32 dQ accumulator set to zero.
-// One warp per row, grid-stride; each lane handles D/32 consecutive elements.
+// D_i = sum_c dO_ic O_ic per row, L_i * log2(e) copied next to it, and the fp32
+// dQ accumulator set to zero.  Both row vectors are padded per head to Npad rows
+// (a multiple of 128) so the main kernels read whole aligned blocks; padding rows
+// get L = +inf (P = 0) and D = 0.  One warp per padded row, grid-stride; each lane
+// handles D/32 consecutive elements.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, long long rows) {
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, long long slots) {
   constexpr int kPer = D / 32;  // 2, 4 or 8 elements per lane
   const int lane = threadIdx.x & 31;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const uint16_t* o = reinterpret_cast<const uint16_t*>(args.o);
   const uint16_t* g = reinterpret_cast<const uint16_t*>(args.dout);
-  for (long long row = warp0; row < rows; row += nwarps) {
+  for (long long slot = warp0; slot < slots; slot += nwarps) {
+    const long long head = slot / args.Npad;
+    const int i = (int)(slot - head * args.Npad);
+    if (i >= args.N) {
+      if (lane == 0) {
+        args.lse_log2[slot] = INFINITY;
+        args.delta[slot] = 0.f;
+      }
+      continue;
+    }
+    const long long row = head * args.N + i;
     const size_t base = (size_t)row * D + lane * kPer;
     float acc = 0.f;
     uint16_t ov[kPer], gv[kPer];
@@ -572,7 +585,10 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, lon
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) args.delta[row] = acc;
+    if (lane == 0) {
+      args.delta[slot] = acc;
+      args.lse_log2[slot] = args.lse[row] * kLog2e;
+    }
     if (args.dq_acc) {
       float* z = args.dq_acc + base;
 #pragma unroll
@@ -594,60 +610,90 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const BwdArgs ar
   }
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
-cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                         const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
+int num_sms() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long rows = (long long)a.BH * a.N;
-  // 1) D and zeroed dQ accumulator
-  {
-    const long long want = (rows + 7) / 8;
-    const int grid = (int)std::min<long long>(want, (long long)sms * 16);
-    fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(a, rows);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  // 2) main kernel
-  {
-    auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, DQB, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
-    if (e != cudaSuccess) return e;
-    const long long nkb = (a.Nk + kBN - 1) / kBN;
-    const long long grid = nkb * a.BHkv * (D / DH);
-    profile_mark_begin(stream);
-    kern<<<(unsigned)grid, kBwdThreads, L::kAlloc, stream>>>(q, k, v, dout, a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    profile_mark_end(stream, 1);
-  }
-  // 3) dQ conversion
-  {
-    const long long n8 = rows * D / 8;
-    const int grid = (int)std::min<long long>((n8 + 255) / 256, (long long)sms * 16);
-    fa_bwd_dq_convert_kernel<BF16><<<grid, 256, 0, stream>>>(a, n8);
-    return cudaGetLastError();
-  }
+  return sms > 0 ? sms : 1;
+}
+
+// D, L log2(e) (both padded per head) and the zeroed dQ accumulator.
+template <int D, bool BF16>
+cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
+  const long long slots = (long long)a.BH * a.Npad;
+  const long long want = (slots + 7) / 8;
+  const int grid = (int)std::min<long long>(want, (long long)num_sms() * 16);
+  fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(a, slots);
+  return cudaGetLastError();
+}
+
+// dQ = scale * dQ accumulator, rounded to the input type.
+template <int D, bool BF16>
+cudaError_t launch_convert(const BwdArgs& a, cudaStream_t stream) {
+  const long long n8 = (long long)a.BH * a.N * D / 8;
+  const int grid = (int)std::min<long long>((n8 + 255) / 256, (long long)num_sms() * 16);
+  fa_bwd_dq_convert_kernel<BF16><<<grid, 256, 0, stream>>>(a, n8);
+  return cudaGetLastError();
+}
+
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
+cudaError_t launch_main(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                        const BwdArgs& a, cudaStream_t stream) {
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
+  auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, DQB, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const long long nkb = (a.Nk + kBN - 1) / kBN;
+  const long long grid = nkb * a.BHkv * (D / DH);
+  profile_mark_begin(stream);
+  kern<<<(unsigned)grid, kBwdThreads, L::kAlloc, stream>>>(q, k, v, dout, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  profile_mark_end(stream, 1);
+  return cudaSuccess;
+}
+
+// The three launches of the backward pass, in order on `stream`.
+template <int D, bool BF16, typename Main>
+cudaError_t launch_all(const BwdArgs& a, cudaStream_t stream, Main main) {
+  cudaError_t e = launch_pre<D, BF16>(a, stream);
+  if (e != cudaSuccess) return e;
+  if ((e = main()) != cudaSuccess) return e;
+  return launch_convert<D, BF16>(a, stream);
 }
 
 }  // namespace
 
-int bwd_query_rows(int d) { return d == 64 ? 128 : 64; }
+int bwd_query_rows(int d) { return d == 256 ? 64 : 128; }
+
+bool bwd_needs_dq_acc(int d) { return d != 128; }
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
     case 64:
-      return bf16 ? launch_bwd_t<64, 64, 128, false, 3, 1, false, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<64, 64, 128, false, 3, 1, false, false>(q, k, v, dout, a, stream);
-    case 128:
-      return bf16 ? launch_bwd_t<128, 128, 64, true, 3, 2, true, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<128, 128, 64, true, 3, 2, true, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_all<64, true>(a, stream, [&] {
+        return launch_main<64, 64, 128, false, 3, 1, false, true>(q, k, v, dout, a, stream);
+      })
+                  : launch_all<64, false>(a, stream, [&] {
+                      return launch_main<64, 64, 128, false, 3, 1, false, false>(q, k, v, dout, a, stream);
+                    });
+    case 128: {
+      // No dQ accumulator: the dQ kernel writes dQ itself, so the pre-pass only
+      // computes D and L log2(e) and no conversion pass follows.
+      BwdArgs a2 = a;
+      a2.dq_acc = nullptr;
+      cudaError_t e = bf16 ? launch_pre<128, true>(a2, stream) : launch_pre<128, false>(a2, stream);
+      if (e != cudaSuccess) return e;
+      return launch_bwd_main_sq(bf16, q, k, v, dout, a2, stream);
+    }
     case 256:
-      return bf16 ? launch_bwd_t<256, 128, 64, true, 1, 1, false, true>(q, k, v, dout, a, stream)
-                  : launch_bwd_t<256, 128, 64, true, 1, 1, false, false>(q, k, v, dout, a, stream);
+      return bf16 ? launch_all<256, true>(a, stream, [&] {
+        return launch_main<256, 128, 64, true, 1, 1, false, true>(q, k, v, dout, a, stream);
+      })
+                  : launch_all<256, false>(a, stream, [&] {
+                      return launch_main<256, 128, 64, true, 1, 1, false, false>(q, k, v, dout, a, stream);
+                    });
     default:
       return cudaErrorInvalidValue;
   }

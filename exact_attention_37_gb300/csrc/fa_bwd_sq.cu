@@ -1,0 +1,680 @@
+// Backward pass for head dimension 128 as two kernels on square 128 x 128 tiles,
+// with no atomics: every gradient element is summed in a fixed order inside one
+// CTA, so dQ, dK and dV are bitwise reproducible.
+//
+// Both kernels rebuild the probabilities block by block from Q, K and the forward
+// pass's logsumexp (page "FlashAttention — فلاش أتنشن", section "Tiling and block
+// processing") and apply the chain-rule derivatives of the attention formula
+// (same page, section "The problem of standard attention"):
+//
+//   P = 2^(S scale log2 e - L log2 e),   dP = dO V^T,   dS = P o (dP - D),
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
+//
+// fa_bwd_kv_kernel: one CTA per (key/value head, 128-key block), looping over the
+//   query blocks of every query head of the group (the key-block parallelism of
+//   page "FlashAttention-2 — فلاش أتنشن-2", section "Technical architecture",
+//   item 2).  Keys sit on TMEM lanes: S^T = K Q^T, dP^T = V dO^T; P^T and dS^T are
+//   written back as packed 16-bit pairs into the columns their fp32 sources came
+//   from and feed dV += P^T dO and dK += dS^T Q as tensor-memory A operands.
+// fa_bwd_q_kernel: one CTA per (query head, 128-row query block), looping over the
+//   key blocks its rows see.  Queries sit on TMEM lanes: S = Q K^T, dP = dO V^T;
+//   dS goes back into the S columns as packed pairs and feeds dQ += dS K; dQ stays
+//   in TMEM until the CTA writes it once, scaled and rounded.
+//
+// The second kernel recomputes S and dP (7 products per tile pair instead of 5);
+// in exchange no fp32 reductions leave the SM, and the dQ accumulator, its
+// zeroing and its conversion pass disappear.
+//
+// Every product has M = N = 128.  Warps: 4 NWG elementwise warps (NWG warpgroups,
+// 128 / NWG tile columns each), one TMA warp, one MMA warp.
+#include <algorithm>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kHd = 128;                  // head dimension
+constexpr uint32_t kPanel = 128 * 128;    // 128 rows x 128 B (64 16-bit columns)
+constexpr uint32_t kTile = 2 * kPanel;    // 128 rows x 128 columns
+
+template <int NWG>
+struct SqCfg {
+  static constexpr int kCols = 128 / NWG;      // tile columns per elementwise thread
+  static constexpr int kCh = kCols / 32;       // 32-column TMEM chunks per thread
+  static constexpr int kEw = 128 * NWG;        // elementwise threads
+  static constexpr int kWarpTma = 4 * NWG;
+  static constexpr int kWarpMma = 4 * NWG + 1;
+  static constexpr int kThreads = kEw + 64;
+  // TMEM column, relative to a packed region, of the 16 K elements of step kk:
+  // warpgroup e packs its kCols columns into kCols / 2 columns starting at kCols e.
+  static constexpr uint32_t packed_col(int kk) { return kCols * ((16 * kk) / kCols) + ((16 * kk) % kCols) / 2; }
+};
+
+__device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+constexpr uint32_t kIdSS(bool bf16) { return make_idesc_f16(bf16, 128, 128, false, false); }  // both K-major
+constexpr uint32_t kIdTS(bool bf16) { return make_idesc_f16(bf16, 128, 128, false, true); }   // A TMEM, B MN-major
+constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand: 8-row groups 1024 B apart
+
+// D (128 x 128, fp32) = A B^T with A, B 128 x 128 K-major tiles in shared memory
+// (two 64-column panels each): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
+  const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, 16);
+#pragma unroll
+  for (int kk = 0; kk < kHd / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
+    mma_ss_lohi(d_tmem, a0 + off, kHi, b0 + off, kHi, idesc, kk > 0);
+  }
+}
+// D (+)= A B with A (128 x 128) packed in TMEM by NWG warpgroups and B a 128 x 128
+// tile in shared memory read MN-major (rows = K, two 64-column panels of N).
+template <int NWG>
+__device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc,
+                                           bool acc) {
+  const uint32_t b0 = sdesc_lo(b_smem, kPanel);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_lohi(d_tmem, a_tmem + SqCfg<NWG>::packed_col(kk), b0 + ((kk * 2048) >> 4), kHi, idesc,
+                (acc || kk > 0) ? 1u : 0u);
+}
+
+// Stores 32 fp32 values (times mul) as 16-bit to dst (64 contiguous bytes).
+template <bool BF16>
+__device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&v)[32], float mul) {
+#pragma unroll
+  for (int x = 0; x < 32; x += 8)
+    st_global_v4(dst + x, pack2<BF16>(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
+                 pack2<BF16>(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
+                 pack2<BF16>(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
+                 pack2<BF16>(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
+}
+
+// ============================================================================ dK, dV
+namespace kv {
+constexpr uint32_t kSmK = 0;
+constexpr uint32_t kSmV = kTile;
+constexpr uint32_t kSmQ = 2 * kTile;   // two stages
+constexpr uint32_t kSmDO = 4 * kTile;  // two stages
+constexpr uint32_t kSmBar = 6 * kTile;
+enum : int {
+  kKVFull = 0,
+  kQFull = 1,    // two
+  kQEmpty = 3,   // two
+  kDOFull = 5,   // two
+  kDOEmpty = 7,  // two
+  kSReady = 9,   // S^T of the block is in TMEM
+  kPFull,        // P^T written
+  kDpReady,      // dP^T of the block is in TMEM
+  kDsFull,       // dS^T written
+  kDone,         // the last dK product has completed
+  kNumBars
+};
+constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
+constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;  // + alignment of the dynamic base
+static_assert(kSmAlloc <= 232448, "shared memory budget");
+constexpr uint32_t kTmS = 0;     // S^T fp32, then P^T packed
+constexpr uint32_t kTmDP = 128;  // dP^T fp32, then dS^T packed
+constexpr uint32_t kTmDV = 256;
+constexpr uint32_t kTmDK = 384;
+}  // namespace kv
+
+template <int NWG, bool BF16>
+__global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
+    fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdArgs args) {
+  using namespace kv;
+  using C = SqCfg<NWG>;
+  constexpr int kCols = C::kCols, kCh = C::kCh;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  auto sQ = [&](int s) -> uint32_t { return sbase + kSmQ + kTile * s; };
+  auto sDO = [&](int s) -> uint32_t { return sbase + kSmDO + kTile * s; };
+  const uint32_t sK = sbase + kSmK, sV = sbase + kSmV;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+  const int Nk = args.Nk;
+
+  // Work tile: lowest key blocks first across all key/value heads (under the causal
+  // mask they see the most query blocks).  The CTA visits the query blocks of every
+  // query head of its key/value head's group, so dK, dV of the group sum in TMEM.
+  const int kb = (int)(blockIdx.x / args.BHkv);
+  const int bh_kv = (int)(blockIdx.x % args.BHkv);
+  const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
+  const int key0 = kb * 128;
+  const int nqb = (N + 127) / 128;
+  const int i_begin = args.causal ? max(0, key0 - koff) / 128 : 0;
+  const int nit_h = nqb - i_begin;  // >= 1: the last query row sees every key
+  const int nit = nit_h * args.group;
+  const int hpb = args.H / args.group;  // key/value heads per batch entry
+  const int bh_q0 = (bh_kv / hpb) * args.H + (bh_kv % hpb) * args.group;
+  auto q_head = [&](int it) { return bh_q0 + it / nit_h; };
+  auto q_block = [&](int it) { return i_begin + it % nit_h; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kKVFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kQFull + s), 1);
+      mbar_init(bar(kQEmpty + s), 1);
+      mbar_init(bar(kDOFull + s), 1);
+      mbar_init(bar(kDOEmpty + s), 1);
+    }
+    mbar_init(bar(kSReady), 1);
+    mbar_init(bar(kPFull), C::kEw);
+    mbar_init(bar(kDpReady), 1);
+    mbar_init(bar(kDsFull), C::kEw);
+    mbar_init(bar(kDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kWarpMma) {
+    tmem_alloc(sbase + kSmTmemSlot, 512);
+    tmem_relinquish();
+  }
+  if (warp == C::kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+
+  if (warp == C::kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(kKVFull), 2 * kTile);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        tma_load_3d(sK + p * kPanel, &tm_k, bar(kKVFull), 64 * p, key0, bh_kv);
+        tma_load_3d(sV + p * kPanel, &tm_v, bar(kKVFull), 64 * p, key0, bh_kv);
+      }
+      int n_do = 0, n_q = 0;  // loads issued
+      for (int it = 0; it < nit; ++it) {
+        const int s = it & 1, u = it >> 1;
+        const int q0 = q_block(it) * 128, bq = q_head(it);
+        // Q first: S^T of a block is issued before its dP^T.
+        if (u > 0 && !mbar_wait(bar(kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(kQFull + s), kTile);
+        tma_load_3d(sQ(s), &tm_q, bar(kQFull + s), 0, q0, bq);
+        tma_load_3d(sQ(s) + kPanel, &tm_q, bar(kQFull + s), 64, q0, bq);
+        ++n_q;
+        if (u > 0 && !mbar_wait(bar(kDOEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(kDOFull + s), kTile);
+        tma_load_3d(sDO(s), &tm_do, bar(kDOFull + s), 0, q0, bq);
+        tma_load_3d(sDO(s) + kPanel, &tm_do, bar(kDOFull + s), 64, q0, bq);
+        ++n_do;
+      }
+      // Every copy this thread issued lands before the CTA exits, even when the
+      // consumers gave up after a timeout elsewhere (bounded waits, abort ignored).
+      mbar_wait(bar(kKVFull), 0, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < 2; ++s) {
+        if (n_q > s) mbar_wait(bar(kQFull + s), ((n_q - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
+        if (n_do > s) mbar_wait(bar(kDOFull + s), ((n_do - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
+      }
+    }
+  } else if (warp == C::kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // Order: S(0) dP(0) | dV(i) S(i+1) dK(i) dP(i+1) | ...  S(i+1) overwrites P^T(i)
+    // only after dV(i) has read it, dP(i+1) overwrites dS^T(i) only after dK(i)
+    // has, because one thread's tcgen05.mma operations execute in issue order.
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(kKVFull), 0, args.err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait(bar(kQFull + 0), 0, args.err, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        mma_scores(tmem + kTmS, sK, sQ(0), kIdSS(BF16));
+        mma_commit(bar(kSReady));
+        ok = mbar_wait(bar(kDOFull + 0), 0, args.err, kErrTimeoutTma);
+      }
+      if (ok) {
+        tc_fence_after();
+        mma_scores(tmem + kTmDP, sV, sDO(0), kIdSS(BF16));
+        mma_commit(bar(kDpReady));
+      }
+      for (int it = 0; ok && it < nit; ++it) {
+        const int s = it & 1, s1 = (it + 1) & 1;
+        if (!(ok = mbar_wait(bar(kPFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_packed<NWG>(tmem + kTmDV, tmem + kTmS, sDO(s), kIdTS(BF16), it > 0);
+        if (it + 1 < nit) {
+          if (!(ok = mbar_wait(bar(kQFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_scores(tmem + kTmS, sK, sQ(s1), kIdSS(BF16));
+          mma_commit(bar(kSReady));
+        }
+        if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_packed<NWG>(tmem + kTmDK, tmem + kTmDP, sQ(s), kIdTS(BF16), it > 0);
+        mma_commit(bar(kQEmpty + s));   // Q(it): last read by dK(it)
+        mma_commit(bar(kDOEmpty + s));  // dO(it): last read by dV(it)
+        if (it + 1 < nit) {
+          if (!(ok = mbar_wait(bar(kDOFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_scores(tmem + kTmDP, sV, sDO(s1), kIdSS(BF16));
+          mma_commit(bar(kDpReady));
+        } else {
+          mma_commit(bar(kDone));
+        }
+      }
+      if (!ok) mma_commit(bar(kDone));  // lets the epilogue wait end; its result is discarded
+      mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
+    }
+  } else {
+    // ------------------------------------------------------------ P^T, dS^T, epilogue
+    const int e = warp >> 2;                 // warpgroup: query columns [kCols e, kCols (e + 1))
+    const int r = ((warp & 3) << 5) + lane;  // TMEM lane: key row
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int cbeg = kCols * e;
+    const int key = key0 + r;
+    const float c = args.scale_log2;
+    // L log2 e and D of block it for this warpgroup's columns (rows padded per head
+    // to a multiple of 128, so whole 16-byte groups are always in bounds).
+    auto lrow = [&](int it) {
+      return args.lse_log2 + (size_t)q_head(it) * args.Npad + q_block(it) * 128 + cbeg;
+    };
+    auto drow = [&](int it) { return args.delta + (size_t)q_head(it) * args.Npad + q_block(it) * 128 + cbeg; };
+    bool ok = true;
+    if (r < 2 * kCh) prefetch_l1((r & 1 ? drow(0) : lrow(0)) + (r >> 1) * 32);
+    for (int it = 0; it < nit; ++it) {
+      const int q0 = q_block(it) * 128;
+      const bool diag = args.causal && (key0 + 127 > q0 + koff);  // some key hidden from some query
+      if (it + 1 < nit && r < 2 * kCh) prefetch_l1((r & 1 ? drow(it + 1) : lrow(it + 1)) + (r >> 1) * 32);
+      // ---- P^T = 2^(S^T c - L log2 e), packed into the S^T columns
+      if (!(ok = mbar_wait(bar(kSReady), it & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+      const float4* L4 = reinterpret_cast<const float4*>(lrow(it));
+      float p[kCols];
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cbeg + 32 * ch, sv);
+        float4 l4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + 8 * ch + i);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        uint32_t pw[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float lv[4] = {l4[i].x, l4[i].y, l4[i].z, l4[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int x = 4 * i + u;
+            float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lv[u]));
+            if (diag && key > q0 + cbeg + 32 * ch + x + koff) pe = 0.f;
+            p[32 * ch + x] = pe;
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[32 * ch + 2 * x], p[32 * ch + 2 * x + 1]);
+        tmem_st_32x32b_x16(tmem + lane_base + kTmS + cbeg + 16 * ch, pw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull));
+      // ---- dS^T = P^T o (dP^T - D), packed into the dP^T columns
+      if (!(ok = mbar_wait(bar(kDpReady), it & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+      const float4* D4 = reinterpret_cast<const float4*>(drow(it));
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv);
+        float4 d4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d4[i] = __ldg(D4 + 8 * ch + i);
+        tmem_wait_ld();
+        reg_fence32(dv);
+        uint32_t dw[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dd[4] = {d4[i].x, d4[i].y, d4[i].z, d4[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            const int x = 4 * i + u;
+            const float ds0 = p[32 * ch + x] * (__uint_as_float(dv[x]) - dd[u]);
+            const float ds1 = p[32 * ch + x + 1] * (__uint_as_float(dv[x + 1]) - dd[u + 1]);
+            dw[x >> 1] = pack2<BF16>(ds0, ds1);
+          }
+        }
+        tmem_st_32x32b_x16(tmem + lane_base + kTmDP + cbeg + 16 * ch, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kDsFull));
+    }
+    // ---- dV, dK of this key block once the last dK product has completed:
+    // lane r holds key row key0 + r, this warpgroup columns [kCols e, kCols (e + 1)).
+    if (ok && mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma)) {
+      tc_fence_after();
+      const size_t out_row = ((size_t)bh_kv * Nk + key) * kHd + cbeg;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = (which == 0 ? kTmDV : kTmDK) + cbeg;
+        const float mul = which == 0 ? 1.f : args.scale;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + out_row;
+#pragma unroll 1
+        for (int ch = 0; ch < kCh; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + col0 + 32 * ch, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (key < Nk) store_row32<BF16>(dst + 32 * ch, v, mul);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================ dQ
+namespace qk {
+constexpr uint32_t kSmQ = 0;
+constexpr uint32_t kSmDO = kTile;
+constexpr uint32_t kSmK = 2 * kTile;   // three stages (K is read by S and by dQ)
+constexpr uint32_t kSmV = 5 * kTile;   // two stages (V is read by dP only)
+constexpr uint32_t kSmBar = 7 * kTile;
+enum : int {
+  kQFull = 0,    // Q and dO
+  kKFull = 1,    // three
+  kKEmpty = 4,   // three
+  kVFull = 7,    // two
+  kVEmpty = 9,   // two
+  kSReady = 11,  // two: S of the block is in TMEM buffer b
+  kDpReady = 13, // dP of the block is in TMEM
+  kDsFull,       // dS written (and dP read)
+  kDone,         // the last dQ product has completed
+  kNumBars
+};
+constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
+constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;
+static_assert(kSmAlloc <= 232448, "shared memory budget");
+constexpr uint32_t kTmS = 0;     // two buffers of 128: S fp32, then dS packed
+constexpr uint32_t kTmDP = 256;  // dP fp32
+constexpr uint32_t kTmDQ = 384;  // dQ accumulator
+}  // namespace qk
+
+template <int NWG, bool BF16>
+__global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
+    fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs args) {
+  using namespace qk;
+  using C = SqCfg<NWG>;
+  constexpr int kCols = C::kCols, kCh = C::kCh;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  auto sK = [&](int s) -> uint32_t { return sbase + kSmK + kTile * s; };
+  auto sV = [&](int s) -> uint32_t { return sbase + kSmV + kTile * s; };
+  const uint32_t sQ = sbase + kSmQ, sDO = sbase + kSmDO;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+  const int Nk = args.Nk;
+
+  // Work tile: the last query blocks first (under the causal mask they see the most
+  // keys), so the final wave holds the lightest work.
+  const int nqb = (N + 127) / 128;
+  const int qb = nqb - 1 - (int)(blockIdx.x / args.BH);
+  const int bh = (int)(blockIdx.x % args.BH);
+  const int bh_kv = (bh / args.H) * (args.H / args.group) + (bh % args.H) / args.group;
+  const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
+  const int q0 = qb * 128;
+  int nkv = (Nk + 127) / 128;
+  if (args.causal) {
+    const int last = min(Nk - 1, q0 + 127 + koff);  // last key any row of the block sees
+    nkv = last < 0 ? 0 : last / 128 + 1;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kSReady + s), 1);
+    }
+    mbar_init(bar(kDpReady), 1);
+    mbar_init(bar(kDsFull), C::kEw);
+    mbar_init(bar(kDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kWarpMma) {
+    tmem_alloc(sbase + kSmTmemSlot, 512);
+    tmem_relinquish();
+  }
+  if (warp == C::kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+
+  if (warp == C::kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nkv > 0) {
+      mbar_expect_tx(bar(kQFull), 2 * kTile);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        tma_load_3d(sQ + p * kPanel, &tm_q, bar(kQFull), 64 * p, q0, bh);
+        tma_load_3d(sDO + p * kPanel, &tm_do, bar(kQFull), 64 * p, q0, bh);
+      }
+      int n_k = 0, n_v = 0;  // loads issued
+      for (int j = 0; j < nkv; ++j) {
+        const int sk = j % 3, uk = j / 3, sv = j & 1, uv = j >> 1;
+        if (uk > 0 && !mbar_wait(bar(kKEmpty + sk), (uk - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(kKFull + sk), kTile);
+        tma_load_3d(sK(sk), &tm_k, bar(kKFull + sk), 0, 128 * j, bh_kv);
+        tma_load_3d(sK(sk) + kPanel, &tm_k, bar(kKFull + sk), 64, 128 * j, bh_kv);
+        ++n_k;
+        if (uv > 0 && !mbar_wait(bar(kVEmpty + sv), (uv - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(kVFull + sv), kTile);
+        tma_load_3d(sV(sv), &tm_v, bar(kVFull + sv), 0, 128 * j, bh_kv);
+        tma_load_3d(sV(sv) + kPanel, &tm_v, bar(kVFull + sv), 64, 128 * j, bh_kv);
+        ++n_v;
+      }
+      // Every copy this thread issued lands before the CTA exits.
+      mbar_wait(bar(kQFull), 0, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < 3; ++s)
+        if (n_k > s) mbar_wait(bar(kKFull + s), ((n_k - 1 - s) / 3) & 1, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < 2; ++s)
+        if (n_v > s) mbar_wait(bar(kVFull + s), ((n_v - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
+    }
+  } else if (warp == C::kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // Order: S(0) dP(0) S(1) | dP(j+1) dQ(j) S(j+2) | ...  dP(j+1) overwrites dP(j)
+    // after the elementwise warps have read it (DsFull), S(j+2) overwrites dS(j) in
+    // buffer j % 2 only after dQ(j) has read it (issue order).
+    if (lane == 0 && nkv > 0) {
+      bool ok = mbar_wait(bar(kQFull), 0, args.err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait(bar(kKFull + 0), 0, args.err, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        mma_scores(tmem + kTmS, sQ, sK(0), kIdSS(BF16));
+        mma_commit(bar(kSReady + 0));
+        ok = mbar_wait(bar(kVFull + 0), 0, args.err, kErrTimeoutTma);
+      }
+      if (ok) {
+        tc_fence_after();
+        mma_scores(tmem + kTmDP, sDO, sV(0), kIdSS(BF16));
+        mma_commit(bar(kDpReady));
+        mma_commit(bar(kVEmpty + 0));
+        if (nkv > 1) {
+          ok = mbar_wait(bar(kKFull + 1), 0, args.err, kErrTimeoutTma);
+          if (ok) {
+            tc_fence_after();
+            mma_scores(tmem + kTmS + 128, sQ, sK(1), kIdSS(BF16));
+            mma_commit(bar(kSReady + 1));
+          }
+        }
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int b = j & 1;
+        if (!(ok = mbar_wait(bar(kDsFull), j & 1, args.err, kErrTimeoutSoftmax))) break;
+        if (j + 1 < nkv) {
+          const int sv1 = (j + 1) & 1;
+          if (!(ok = mbar_wait(bar(kVFull + sv1), ((j + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_scores(tmem + kTmDP, sDO, sV(sv1), kIdSS(BF16));
+          mma_commit(bar(kDpReady));
+          mma_commit(bar(kVEmpty + sv1));
+        }
+        tc_fence_after();
+        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmS + 128 * b, sK(j % 3), kIdTS(BF16), j > 0);
+        mma_commit(bar(kKEmpty + j % 3));  // K(j): last read by dQ(j)
+        if (j + 2 < nkv) {
+          const int sk2 = (j + 2) % 3;
+          if (!(ok = mbar_wait(bar(kKFull + sk2), ((j + 2) / 3) & 1, args.err, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_scores(tmem + kTmS + 128 * b, sQ, sK(sk2), kIdSS(BF16));
+          mma_commit(bar(kSReady + b));
+        }
+      }
+      mma_commit(bar(kDone));
+      mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
+    }
+  } else {
+    // ------------------------------------------------------------ P, dS, epilogue
+    const int e = warp >> 2;                 // warpgroup: key columns [kCols e, kCols (e + 1))
+    const int r = ((warp & 3) << 5) + lane;  // TMEM lane: query row
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int cbeg = kCols * e;
+    const int q = q0 + r;
+    const float c = args.scale_log2;
+    const float Lr = args.lse_log2[(size_t)bh * args.Npad + q];  // +inf on padding rows: P = 0
+    const float Dr = args.delta[(size_t)bh * args.Npad + q];
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j & 1;
+      const int k0 = 128 * j;
+      const bool diag = args.causal && (k0 + 127 > q0 + koff);  // some key hidden from some query
+      // ---- P = 2^(S c - L log2 e), kept in registers
+      if (!(ok = mbar_wait(bar(kSReady + b), (j >> 1) & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+      float p[kCols];
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 128 * b + cbeg + 32 * ch, sv);
+        tmem_wait_ld();
+        reg_fence32(sv);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -Lr));
+          if (diag && k0 + cbeg + 32 * ch + x > q + koff) pe = 0.f;
+          p[32 * ch + x] = pe;
+        }
+      }
+      // ---- dS = P o (dP - D), packed into the S columns of buffer b
+      if (!(ok = mbar_wait(bar(kDpReady), j & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv);
+        tmem_wait_ld();
+        reg_fence32(dv);
+        uint32_t dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const float ds0 = p[32 * ch + x] * (__uint_as_float(dv[x]) - Dr);
+          const float ds1 = p[32 * ch + x + 1] * (__uint_as_float(dv[x + 1]) - Dr);
+          dw[x >> 1] = pack2<BF16>(ds0, ds1);
+        }
+        tmem_st_32x32b_x16(tmem + lane_base + kTmS + 128 * b + cbeg + 16 * ch, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kDsFull));
+    }
+    // ---- dQ rows: lane r holds query row q, this warpgroup columns [kCols e, kCols (e + 1)).
+    if (ok && (nkv == 0 || mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
+      tc_fence_after();
+      uint16_t* dst = reinterpret_cast<uint16_t*>(args.dq) + ((size_t)bh * N + q) * kHd + cbeg;
+#pragma unroll 1
+      for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t v[32];
+        if (nkv > 0) {
+          tmem_ld_32x32b_x32(tmem + lane_base + kTmDQ + cbeg + 32 * ch, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] = 0u;  // rows that see no key: dQ = 0
+        }
+        if (q < N) store_row32<BF16>(dst + 32 * ch, v, args.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+#ifndef FA_BWD_SQ_NWG
+#define FA_BWD_SQ_NWG 4
+#endif
+
+template <bool BF16>
+cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                      const BwdArgs& a, cudaStream_t stream) {
+  constexpr int kNwg = FA_BWD_SQ_NWG;
+  constexpr int kThreads = SqCfg<kNwg>::kThreads;
+  auto kkv = fa_bwd_kv_kernel<kNwg, BF16>;
+  auto kq = fa_bwd_q_kernel<kNwg, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv::kSmAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::kSmAlloc);
+  if (e != cudaSuccess) return e;
+  const long long grid_kv = (long long)((a.Nk + 127) / 128) * a.BHkv;
+  const long long grid_q = (long long)((a.N + 127) / 128) * a.BH;
+  profile_mark_begin(stream);
+  kkv<<<(unsigned)grid_kv, kThreads, kv::kSmAlloc, stream>>>(q, k, v, dout, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kq<<<(unsigned)grid_q, kThreads, qk::kSmAlloc, stream>>>(q, k, v, dout, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_mark_end(stream, 1);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_sq(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
+  return bf16 ? launch_sq<true>(q, k, v, dout, a, stream) : launch_sq<false>(q, k, v, dout, a, stream);
+}
+
+}  // namespace fa

@@ -28,11 +28,13 @@ struct BwdArgs {
   const void* dout;      // [B*H, N, d] upstream gradient (16-bit)
   const float* lse;      // [B*H, N] logsumexp from the forward pass
   float* dq_acc;         // [B*H, N, d] fp32 dQ accumulator (workspace)
-  float* delta;          // [B*H, N] fp32 D = rowsum(dO o O) (workspace)
+  float* lse_log2;       // [B*H, Npad] L * log2(e), +inf on padding rows (workspace)
+  float* delta;          // [B*H, Npad] fp32 D = rowsum(dO o O), 0 on padding rows (workspace)
   void* dq;              // [B*H, N, d] 16-bit dQ output
-  void* dk;              // [B*H, N, d] 16-bit dK output
-  void* dv;              // [B*H_kv, Nk, d] 16-bit dV output (dk likewise)
+  void* dk;              // [B*H_kv, Nk, d] 16-bit dK output
+  void* dv;              // [B*H_kv, Nk, d] 16-bit dV output
   int N;                 // query rows per head (N_q)
+  int Npad;              // N rounded up to a multiple of 128 (row stride of lse_log2 and delta)
   int Nk;                // key/value rows per head (N_k)
   int d;
   int BH;                // batch * query heads
@@ -54,6 +56,22 @@ cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
 // Measurement hook: events around a main kernel while profiling is on (no-ops otherwise).
 void profile_mark_begin(cudaStream_t stream);
 void profile_mark_end(cudaStream_t stream, int kind);
+
+// Whether the backward pass for head dimension d accumulates dQ in an fp32
+// workspace buffer (reductions from every key block) or writes dQ directly.
+bool bwd_needs_dq_acc(int d);
+
+// Workspace layout of the backward pass (bytes): the dQ accumulator (if the head
+// dimension needs one), then L*log2(e) and D rows padded per head to a multiple
+// of 128, each part 256-byte aligned.
+size_t bwd_workspace_bytes(long long BH, int N, int d);
+size_t bwd_lse_offset(long long BH, int N, int d);
+size_t bwd_delta_offset(long long BH, int N, int d);
+inline int bwd_npad(int N) { return (N + 127) / 128 * 128; }
+
+// Main kernels of the backward pass with 128 x 128 tiles (d = 128): dK/dV, then dQ.
+cudaError_t launch_bwd_main_sq(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);

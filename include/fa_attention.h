@@ -91,8 +91,12 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
- * Bytes of device workspace `fa_bwd` needs: an fp32 dQ accumulator [B,H,N,d],
- * the fp32 row vector D [B,H,N], and alignment padding.  Linear in N.
+ * Bytes of device workspace `fa_bwd` needs: for d = 64 and d = 256 an fp32 dQ
+ * accumulator [B,H,N,d] (those head dimensions sum dQ with reductions from
+ * every key block), then two fp32 row vectors (L log2 e and D = rowsum(dO o O))
+ * whose rows are padded per head to a multiple of 128, each part 256-byte
+ * aligned.  Linear in N: about B*H*N*(4d + 8) bytes, or B*H*N*8 for d = 128,
+ * whose dQ kernel keeps its accumulator on chip.
  * Returns 0 for invalid or empty sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -111,8 +115,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace    : device buffer of at least fa_bwd_workspace_size(B,H,N,d)
  *                  bytes, 256-byte aligned; contents need not be initialised
  *                  and are overwritten.
- * Launches, in order on `stream`: the D pre-pass (which also zeroes the dQ
- * accumulator), the key-block-parallel main kernel, and the dQ conversion.
+ * Launches, in order on `stream`: the pre-pass (D and L log2 e; for d = 64
+ * and 256 it also zeroes the dQ accumulator), then for d = 128 a
+ * key-block-parallel dK/dV kernel and a query-block-parallel dQ kernel, for
+ * d = 64 and 256 one key-block-parallel kernel (dK, dV, and dQ by fp32
+ * reductions into the accumulator) and the dQ conversion.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
@@ -125,9 +132,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * per key block, without atomics on dK/dV).  The workspace is
  * fa_bwd_workspace_size(B, H, N_q, d) bytes.  With B*H*N_q == 0 no query
  * row exists, so dk and dv are set to zero (cudaMemsetAsync on `stream`).
- * dK and dV are deterministic (one CTA sums each key row in a fixed order);
- * dQ accumulates fp32 reductions from every key block, so its last bits depend
- * on scheduling.
+ * dK and dV are deterministic (one CTA sums each key row in a fixed order).
+ * For d = 128 dQ is deterministic too (one CTA sums each query row over the
+ * key blocks in a fixed order): repeated calls give bitwise equal gradients.
+ * For d = 64 and 256 dQ accumulates fp32 reductions from every key block, so
+ * its last bits depend on scheduling.
  * fa_bwd(..., N, ...) is fa_bwd_ex with H_kv = H and N_q = N_k = N.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -143,12 +152,13 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * counterpart to this entry point; it only changes where the scratch lives.)
  *
  * Arguments, layout, results and errors are those of fa_bwd, minus the
- * workspace pair.  The scratch (the fp32 dQ accumulator and the fp32 D rows,
- * fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
+ * workspace pair.  The scratch (the fp32 dQ accumulator and the fp32 row
+ * vectors, fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
  * library's device memory, allocated when the library's device code is loaded
  * and held by every GPU that loads it until the process exits.  Calls whose
  * scratch would exceed 32 MiB (33554432 bytes) return FA_ERR_WORKSPACE and
- * launch nothing; with d = 128 that is B*H*N up to 65,027 rows.
+ * launch nothing; with B*H = 1 that is N up to 127,100 rows at d = 64 and
+ * 4,194,304 rows at d = 128.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.  No
