@@ -85,6 +85,18 @@ __device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uin
                 (acc || kk > 0) ? 1u : 0u);
 }
 
+// D (+)= A B with A (128 x 128) a K-major tile in shared memory (rows = M, two
+// 64-column panels of K) and B read MN-major as in mma_packed.
+__device__ __forceinline__ void mma_kmajor_a(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
+                                             bool acc) {
+  const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, kPanel);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t a_off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
+    mma_ss_lohi(d_tmem, a0 + a_off, kHi, b0 + ((kk * 2048) >> 4), kHi, idesc, (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
 // Stores 32 fp32 values (times mul) as 16-bit to dst (64 contiguous bytes).
 template <bool BF16>
 __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&v)[32], float mul) {
@@ -102,7 +114,8 @@ constexpr uint32_t kSmK = 0;
 constexpr uint32_t kSmV = kTile;
 constexpr uint32_t kSmQ = 2 * kTile;   // two stages
 constexpr uint32_t kSmDO = 4 * kTile;  // two stages
-constexpr uint32_t kSmBar = 6 * kTile;
+constexpr uint32_t kSmPt = 6 * kTile;  // P^T, 128 keys x 128 queries, K-major, two 64-query panels
+constexpr uint32_t kSmBar = 7 * kTile;
 enum : int {
   kKVFull = 0,
   kQFull = 1,    // two
@@ -110,7 +123,8 @@ enum : int {
   kDOFull = 5,   // two
   kDOEmpty = 7,  // two
   kSReady = 9,   // S^T of the block is in TMEM
-  kPFull,        // P^T written
+  kPFull,        // S^T read out and P^T written to shared memory
+  kPtFree,       // dV has read P^T
   kDpReady,      // dP^T of the block is in TMEM
   kDsFull,       // dS^T written
   kDone,         // the last dK product has completed
@@ -119,7 +133,7 @@ enum : int {
 constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
 constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;  // + alignment of the dynamic base
 static_assert(kSmAlloc <= 232448, "shared memory budget");
-constexpr uint32_t kTmS = 0;     // S^T fp32, then P^T packed
+constexpr uint32_t kTmS = 0;     // S^T fp32
 constexpr uint32_t kTmDP = 128;  // dP^T fp32, then dS^T packed
 constexpr uint32_t kTmDV = 256;
 constexpr uint32_t kTmDK = 384;
@@ -139,7 +153,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
   auto sQ = [&](int s) -> uint32_t { return sbase + kSmQ + kTile * s; };
   auto sDO = [&](int s) -> uint32_t { return sbase + kSmDO + kTile * s; };
-  const uint32_t sK = sbase + kSmK, sV = sbase + kSmV;
+  const uint32_t sK = sbase + kSmK, sV = sbase + kSmV, sPt = sbase + kSmPt;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -171,9 +185,10 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       mbar_init(bar(kDOEmpty + s), 1);
     }
     mbar_init(bar(kSReady), 1);
-    mbar_init(bar(kPFull), C::kEw);
+    mbar_init(bar(kPFull), C::kEw / 32);  // one arrival per elementwise warp
+    mbar_init(bar(kPtFree), 1);
     mbar_init(bar(kDpReady), 1);
-    mbar_init(bar(kDsFull), C::kEw);
+    mbar_init(bar(kDsFull), C::kEw / 32);
     mbar_init(bar(kDone), 1);
     fence_mbar_init();
   }
@@ -227,9 +242,10 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     }
   } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Order: S(0) dP(0) | dV(i) S(i+1) dK(i) dP(i+1) | ...  S(i+1) overwrites P^T(i)
-    // only after dV(i) has read it, dP(i+1) overwrites dS^T(i) only after dK(i)
-    // has, because one thread's tcgen05.mma operations execute in issue order.
+    // Order: S(0) dP(0) | S(i+1) dV(i) dK(i) dP(i+1) | ...  S(i+1) follows as soon
+    // as S^T(i) has been read out (P^T(i) is in shared memory); dP(i+1) overwrites
+    // dS^T(i) only after dK(i) has read it, because one thread's tcgen05.mma
+    // operations execute in issue order.
     if (lane == 0) {
       bool ok = mbar_wait(bar(kKVFull), 0, args.err, kErrTimeoutTma);
       if (ok) ok = mbar_wait(bar(kQFull + 0), 0, args.err, kErrTimeoutTma);
@@ -248,13 +264,14 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         const int s = it & 1, s1 = (it + 1) & 1;
         if (!(ok = mbar_wait(bar(kPFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_packed<NWG>(tmem + kTmDV, tmem + kTmS, sDO(s), kIdTS(BF16), it > 0);
         if (it + 1 < nit) {
           if (!(ok = mbar_wait(bar(kQFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
           mma_scores(tmem + kTmS, sK, sQ(s1), kIdSS(BF16));
           mma_commit(bar(kSReady));
         }
+        mma_kmajor_a(tmem + kTmDV, sPt, sDO(s), kIdTS(BF16), it > 0);
+        mma_commit(bar(kPtFree));
         if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_packed<NWG>(tmem + kTmDK, tmem + kTmDP, sQ(s), kIdTS(BF16), it > 0);
@@ -292,41 +309,60 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       const int q0 = q_block(it) * 128;
       const bool diag = args.causal && (key0 + 127 > q0 + koff);  // some key hidden from some query
       if (it + 1 < nit && r < 2 * kCh) prefetch_l1((r & 1 ? drow(it + 1) : lrow(it + 1)) + (r >> 1) * 32);
-      // ---- P^T = 2^(S^T c - L log2 e), packed into the S^T columns
-      if (!(ok = mbar_wait(bar(kSReady), it & 1, args.err, kErrTimeoutMma))) break;
-      tc_fence_after();
+      // ---- P^T = 2^(S^T c - L log2 e), packed into the S^T columns.  The first
+      // chunk's L values are requested before the wait, so their latency hides in it.
       const float4* L4 = reinterpret_cast<const float4*>(lrow(it));
+      float4 l4[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + i);
+      if (!(ok = warp_wait(bar(kSReady), it & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
       float p[kCols];
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         uint32_t sv[32];
         tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cbeg + 32 * ch, sv);
-        float4 l4[8];
+        if (ch > 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + 8 * ch + i);
+          for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + 8 * ch + i);
+        }
         tmem_wait_ld();
         reg_fence32(sv);
-        uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float lv[4] = {l4[i].x, l4[i].y, l4[i].z, l4[i].w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int x = 4 * i + u;
-            float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lv[u]));
-            if (diag && key > q0 + cbeg + 32 * ch + x + koff) pe = 0.f;
-            p[32 * ch + x] = pe;
-          }
+          const int x = 4 * i;
+          float x0, x1, x2, x3;
+          fma2v(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), c, -l4[i].x, -l4[i].y, x0, x1);
+          fma2v(__uint_as_float(sv[x + 2]), __uint_as_float(sv[x + 3]), c, -l4[i].z, -l4[i].w, x2, x3);
+          p[32 * ch + x] = ex2_approx(x0);
+          p[32 * ch + x + 1] = ex2_approx(x1);
+          p[32 * ch + x + 2] = ex2_approx(x2);
+          p[32 * ch + x + 3] = ex2_approx(x3);
         }
+        if (diag) {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[32 * ch + 2 * x], p[32 * ch + 2 * x + 1]);
-        tmem_st_32x32b_x16(tmem + lane_base + kTmS + cbeg + 16 * ch, pw);
+          for (int x = 0; x < 32; ++x)
+            if (key > q0 + cbeg + 32 * ch + x + koff) p[32 * ch + x] = 0.f;
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kPFull));
+      tc_fence_before();  // S^T has been read out of TMEM
+      // P^T to shared memory (K-major, key row r), once dV of the previous block has read it.
+      if (it > 0 && !(ok = warp_wait(bar(kPtFree), (it - 1) & 1, args.err, kErrTimeoutMma))) break;
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        const uint32_t panel = sPt + (uint32_t)(cbeg / 64) * kPanel;
+        const int c0 = (cbeg % 64 + 32 * ch) / 8;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float* pp = p + 32 * ch + 8 * k4;
+          st_shared_v4(panel + sw128_offset(r, c0 + k4), pack2<BF16>(pp[0], pp[1]), pack2<BF16>(pp[2], pp[3]),
+                       pack2<BF16>(pp[4], pp[5]), pack2<BF16>(pp[6], pp[7]));
+        }
+      }
+      fence_proxy_async_smem();
+      warp_arrive(bar(kPFull));
       // ---- dS^T = P^T o (dP^T - D), packed into the dP^T columns
-      if (!(ok = mbar_wait(bar(kDpReady), it & 1, args.err, kErrTimeoutMma))) break;
+      if (!(ok = warp_wait(bar(kDpReady), it & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
       const float4* D4 = reinterpret_cast<const float4*>(drow(it));
 #pragma unroll
@@ -341,24 +377,24 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         uint32_t dw[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float dd[4] = {d4[i].x, d4[i].y, d4[i].z, d4[i].w};
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            const int x = 4 * i + u;
-            const float ds0 = p[32 * ch + x] * (__uint_as_float(dv[x]) - dd[u]);
-            const float ds1 = p[32 * ch + x + 1] * (__uint_as_float(dv[x + 1]) - dd[u + 1]);
-            dw[x >> 1] = pack2<BF16>(ds0, ds1);
-          }
+          const int x = 4 * i;
+          float ds0, ds1, ds2, ds3;
+          submul2(p[32 * ch + x], p[32 * ch + x + 1], __uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), d4[i].x,
+                  d4[i].y, ds0, ds1);
+          submul2(p[32 * ch + x + 2], p[32 * ch + x + 3], __uint_as_float(dv[x + 2]), __uint_as_float(dv[x + 3]),
+                  d4[i].z, d4[i].w, ds2, ds3);
+          dw[x >> 1] = pack2<BF16>(ds0, ds1);
+          dw[(x >> 1) + 1] = pack2<BF16>(ds2, ds3);
         }
         tmem_st_32x32b_x16(tmem + lane_base + kTmDP + cbeg + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kDsFull));
+      warp_arrive(bar(kDsFull));
     }
     // ---- dV, dK of this key block once the last dK product has completed:
     // lane r holds key row key0 + r, this warpgroup columns [kCols e, kCols (e + 1)).
-    if (ok && mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma)) {
+    if (ok && warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma)) {
       tc_fence_after();
       const size_t out_row = ((size_t)bh_kv * Nk + key) * kHd + cbeg;
 #pragma unroll 1
@@ -401,8 +437,9 @@ enum : int {
   kVEmpty = 9,   // two
   kSReady = 11,  // two: S of the block is in TMEM buffer b
   kDpReady = 13, // dP of the block is in TMEM
-  kDsFull,       // dS written (and dP read)
-  kDone,         // the last dQ product has completed
+  kDpRead = 14,  // dP of the block has been read out of TMEM
+  kDsFull = 15,  // two, used alternately: dS of the block written into buffer b
+  kDone = 17,    // the last dQ product has completed
   kNumBars
 };
 constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
@@ -460,7 +497,9 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       mbar_init(bar(kSReady + s), 1);
     }
     mbar_init(bar(kDpReady), 1);
-    mbar_init(bar(kDsFull), C::kEw);
+    mbar_init(bar(kDpRead), C::kEw / 32);  // one arrival per elementwise warp
+    mbar_init(bar(kDsFull + 0), C::kEw / 32);
+    mbar_init(bar(kDsFull + 1), C::kEw / 32);
     mbar_init(bar(kDone), 1);
     fence_mbar_init();
   }
@@ -512,8 +551,9 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     // Order: S(0) dP(0) S(1) | dP(j+1) dQ(j) S(j+2) | ...  dP(j+1) overwrites dP(j)
-    // after the elementwise warps have read it (DsFull), S(j+2) overwrites dS(j) in
-    // buffer j % 2 only after dQ(j) has read it (issue order).
+    // as soon as the elementwise warps have read it out (DpRead), while they still
+    // compute dS(j); S(j+2) overwrites dS(j) in buffer j % 2 only after dQ(j) has
+    // read it (issue order).
     if (lane == 0 && nkv > 0) {
       bool ok = mbar_wait(bar(kQFull), 0, args.err, kErrTimeoutTma);
       if (ok) ok = mbar_wait(bar(kKFull + 0), 0, args.err, kErrTimeoutTma);
@@ -539,7 +579,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const int b = j & 1;
-        if (!(ok = mbar_wait(bar(kDsFull), j & 1, args.err, kErrTimeoutSoftmax))) break;
+        if (!(ok = mbar_wait(bar(kDpRead), j & 1, args.err, kErrTimeoutSoftmax))) break;
         if (j + 1 < nkv) {
           const int sv1 = (j + 1) & 1;
           if (!(ok = mbar_wait(bar(kVFull + sv1), ((j + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
@@ -548,6 +588,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
           mma_commit(bar(kDpReady));
           mma_commit(bar(kVEmpty + sv1));
         }
+        if (!(ok = mbar_wait(bar(kDsFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_packed<NWG>(tmem + kTmDQ, tmem + kTmS + 128 * b, sK(j % 3), kIdTS(BF16), j > 0);
         mma_commit(bar(kKEmpty + j % 3));  // K(j): last read by dQ(j)
@@ -578,7 +619,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       const int k0 = 128 * j;
       const bool diag = args.causal && (k0 + 127 > q0 + koff);  // some key hidden from some query
       // ---- P = 2^(S c - L log2 e), kept in registers
-      if (!(ok = mbar_wait(bar(kSReady + b), (j >> 1) & 1, args.err, kErrTimeoutMma))) break;
+      if (!(ok = warp_wait(bar(kSReady + b), (j >> 1) & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
       float p[kCols];
 #pragma unroll
@@ -588,36 +629,47 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         tmem_wait_ld();
         reg_fence32(sv);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          float pe = ex2_approx(fmaf(__uint_as_float(sv[x]), c, -Lr));
-          if (diag && k0 + cbeg + 32 * ch + x > q + koff) pe = 0.f;
-          p[32 * ch + x] = pe;
+        for (int x = 0; x < 32; x += 2) {
+          float x0, x1;
+          fma2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), c, -Lr, x0, x1);
+          p[32 * ch + x] = ex2_approx(x0);
+          p[32 * ch + x + 1] = ex2_approx(x1);
+        }
+        if (diag) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (k0 + cbeg + 32 * ch + x > q + koff) p[32 * ch + x] = 0.f;
         }
       }
       // ---- dS = P o (dP - D), packed into the S columns of buffer b
-      if (!(ok = mbar_wait(bar(kDpReady), j & 1, args.err, kErrTimeoutMma))) break;
+      if (!(ok = warp_wait(bar(kDpReady), j & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
+      uint32_t dv[kCh][32];
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv[ch]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) reg_fence32(dv[ch]);
+      tc_fence_before();
+      warp_arrive(bar(kDpRead));  // the next dP may overwrite these columns now
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
-        uint32_t dv[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv);
-        tmem_wait_ld();
-        reg_fence32(dv);
         uint32_t dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const float ds0 = p[32 * ch + x] * (__uint_as_float(dv[x]) - Dr);
-          const float ds1 = p[32 * ch + x + 1] * (__uint_as_float(dv[x + 1]) - Dr);
+          float ds0, ds1;
+          submul2(p[32 * ch + x], p[32 * ch + x + 1], __uint_as_float(dv[ch][x]), __uint_as_float(dv[ch][x + 1]), Dr,
+                  Dr, ds0, ds1);
           dw[x >> 1] = pack2<BF16>(ds0, ds1);
         }
         tmem_st_32x32b_x16(tmem + lane_base + kTmS + 128 * b + cbeg + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kDsFull));
+      warp_arrive(bar(kDsFull + b));
     }
     // ---- dQ rows: lane r holds query row q, this warpgroup columns [kCols e, kCols (e + 1)).
-    if (ok && (nkv == 0 || mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
+    if (ok && (nkv == 0 || warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
       tc_fence_after();
       uint16_t* dst = reinterpret_cast<uint16_t*>(args.dq) + ((size_t)bh * N + q) * kHd + cbeg;
 #pragma unroll 1

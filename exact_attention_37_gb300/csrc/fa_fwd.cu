@@ -120,7 +120,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     }
     for (int t = 0; t < NQ; ++t) {
       mbar_init(bar(L::kSFull + t), 1);
-      mbar_init(bar(L::kPFull + t), kBM);
+      mbar_init(bar(L::kPFull + t), kBM / 32);  // one arrival per softmax warp
       mbar_init(bar(L::kODone + t), 1);
     }
     mbar_init(bar(L::kDrain), 1);
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     bool ok = true;
     const int my_blocks = nblk[t];
     for (int j = 0; j < my_blocks; ++j) {
-      ok = mbar_wait(bar(L::kSFull + t), j & 1, args.err, kErrTimeoutMma);
+      ok = warp_wait(bar(L::kSFull + t), j & 1, args.err, kErrTimeoutMma);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       tmem_wait_st();
       // O_t is rescaled only when the reference moved, after the previous P V is done.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = mbar_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
+        ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
@@ -313,15 +313,15 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(bar(L::kPFull + t));
+      warp_arrive(bar(L::kPFull + t));
       m = m_use;
     }
     const bool has_rows = row0 + kBM * t < N;
     if (ok && has_rows) {
       // A sub-tile whose rows see no key at all writes O = 0 and L = -inf; it still
       // waits for its Q tile to land before reusing that shared memory.
-      ok = my_blocks > 0 ? mbar_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma)
-                         : mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
+      ok = my_blocks > 0 ? warp_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma)
+                         : warp_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

@@ -94,6 +94,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// Warp-uniform bounded wait: every lane waits, and every lane sees a failure if
+// any lane's wait gave up, so a warp never splits between the two paths (a later
+// warp-wide operation would otherwise wait for lanes that left).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, code));
+}
+// One arrival per warp (the barrier counts warps): __syncwarp orders every lane's
+// earlier operations, fences included, before lane 0's arrive.  Arriving threads
+// contend for one shared-memory word, so a warp arrives once, not 32 times.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // A barrier among `count` threads built on an mbarrier, so that its wait is
 // bounded like every other wait: each thread arrives, then waits for the phase.
 struct SmemSync {
@@ -278,6 +292,21 @@ __device__ __forceinline__ void fma2(float a0, float a1, float b, float c, float
       " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) = (a0 * b + c0, a1 * b + c1) with one packed f32x2 FMA.
+__device__ __forceinline__ void fma2v(float a0, float a1, float b, float c0, float c1, float& d0, float& d1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n mov.b64 c, {%5, %6};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (p0 * (a0 - b0), p1 * (a1 - b1)) with a packed f32x2 subtract and multiply.
+__device__ __forceinline__ void submul2(float p0, float p1, float a0, float a1, float b0, float b1, float& d0,
+                                        float& d1) {
+  asm("{\n .reg .b64 p, a, b, d;\n mov.b64 p, {%2, %3};\n mov.b64 a, {%4, %5};\n mov.b64 b, {%6, %7};\n"
+      " sub.f32x2 d, a, b;\n mul.f32x2 d, p, d;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(p0), "f"(p1), "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 // (d0, d1) += (a0, a1) with one packed f32x2 add.
 __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
