@@ -393,7 +393,9 @@ def main():
     bwd_main_avg = statistics.mean(bwd_main_ms) if bwd_main_ms else 0.0
     flops_bwd = attention_flops(w) - flops_fwd
     if bwd_main_avg >= fwd_avg:
-        dom, dom_ms, dom_flops = "fa_bwd_kernel", bwd_main_avg, flops_bwd
+        # the main backward launches between the library's marks: dK/dV + dQ kernels
+        # for d = 128, the fused kernel otherwise
+        dom, dom_ms, dom_flops = "fa_bwd_main", bwd_main_avg, flops_bwd
     else:
         dom, dom_ms, dom_flops = "fa_fwd_kernel", fwd_avg, flops_fwd
     tag = f"{dom}_{profile_key}"
@@ -417,7 +419,8 @@ def main():
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-                       "step": "fwd" if fwd_only else "fwd + bwd (pre, main, dq convert)",
+                       "step": "fwd" if fwd_only else ("fwd + bwd (pre, dK/dV kernel, dQ kernel)" if d == 128
+                                                        else "fwd + bwd (pre, main, dq convert)"),
                        "l2": "256 MB flush write before every step", "parallelism": f"replicas x{world}"},
             "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"])},
             "bwd": None if fwd_only else {

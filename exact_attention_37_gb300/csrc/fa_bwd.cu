@@ -1,4 +1,7 @@
-// Backward pass of exact attention for sm_103a.
+// Backward pass of exact attention for sm_103a: the pre-pass and dQ conversion
+// kernels, the launch sequence for every head dimension, and the fused main
+// kernel used for d = 64 and d = 256 (d = 128 runs the two deterministic main
+// kernels of fa_bwd_sq.cu instead).
 //
 // The pages say the method serves training (page "FlashAttention-2 —
 // فلاش أتنشن-2", section "Performance and efficiency") and that no N x N matrix
@@ -52,7 +55,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // DQT: compute dQ^T (M = DH) instead of dQ (M = BM); STG: Q/dO pipeline depth;
 // NPB: P^T/dS^T tile buffers (2 lets the softmax warps write block i+1 while the
 // tensor cores still read block i).
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB>
 struct BwdLayout {
   static constexpr uint32_t kKVPanel = kBN * 128;                 // 128 key rows x 128 B
   static constexpr uint32_t kQPanel = BM * 128;                   // BM query rows x 128 B
@@ -66,11 +69,7 @@ struct BwdLayout {
   static constexpr uint32_t kDs = kQ + STG * 2 * kQTile;          // NPB x dS^T
   static constexpr uint32_t dst(int b) { return kDs + kPdsTile * b; }
   static constexpr uint32_t kLD = kDs + kPdsTile * NPB;           // 2 buffers x (L, D) x BM floats
-  // dQ staging (DQB, with dQ^T): BM query rows of DH fp32, transposed through shared
-  // memory so the accumulation can use 128-bit reductions.
-  static constexpr uint32_t kDqRowBytes = DH * 4;
-  static constexpr uint32_t kDqStage = kLD + 2 * 2 * BM * 4;
-  static constexpr uint32_t kBar = kDqStage + (DQB ? BM * kDqRowBytes : 0);
+  static constexpr uint32_t kBar = kLD + 2 * 2 * BM * 4;
   static constexpr int kKVFull = 0;
   static constexpr int kQFull = 1;
   static constexpr int kQEmpty = kQFull + STG;
@@ -83,8 +82,7 @@ struct BwdLayout {
   static constexpr int kDqFree = kGrads + NPB;
   static constexpr int kDrain = kDqFree + 1;
   static constexpr int kEwSync = kDrain + 1;                      // two: one per elementwise warpgroup
-  static constexpr int kWqSync = kEwSync + 2;                     // the dQ warpgroup
-  static constexpr int kNumBars = kWqSync + 1;
+  static constexpr int kNumBars = kEwSync + 2;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -111,19 +109,16 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 __device__ __forceinline__ void red_add(float* addr, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdArgs args) {
-  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
   constexpr int kHalves = D / DH;
   constexpr int kCW = BM / 2;        // query columns per elementwise warpgroup
   constexpr int kNCh = kCW / 32;     // 32-column TMEM chunks per elementwise thread
@@ -181,7 +176,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kDrain), 1);
     mbar_init(bar(L::kEwSync + 0), 128);
     mbar_init(bar(L::kEwSync + 1), 128);
-    mbar_init(bar(L::kWqSync), 128);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -442,7 +436,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = (wq << 5) + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     bool ok = true;
-    SmemSync wq_sync{bar(L::kWqSync), 0u};
     for (int it = 0; it < nit; ++it) {
       const int q0 = q_block(it) * BM;
       float* dq_acc = args.dq_acc + (size_t)q_head(it) * N * D;
@@ -458,30 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int ch = 0; ch < kCh; ++ch) reg_fence32(v[ch]);
       tc_fence_before();
       mbar_arrive(bar(L::kDqFree));
-      if constexpr (DQB && DQT) {
-        // dQ^T gives each lane one column of the block's dQ rows.  Transpose it
-        // through shared memory so every thread then owns 16-byte pieces of rows
-        // and the accumulation uses 128-bit reductions (a quarter of the
-        // instructions of per-column ones).
-        const uint32_t stg = sbase + L::kDqStage;
-        if (!(ok = wq_sync.sync(args.err))) break;  // the previous block's staged rows have been read
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch)
-#pragma unroll
-          for (int x = 0; x < 32; ++x) st_shared_f32(stg + (32 * ch + x) * L::kDqRowBytes + 4 * r, v[ch][x]);
-        if (!(ok = wq_sync.sync(args.err))) break;
-        constexpr int kV4PerRow = DH / 4;
-#pragma unroll 4
-        for (int j = r; j < BM * kV4PerRow; j += 128) {
-          const int row = j / kV4PerRow, c4 = j % kV4PerRow;
-          if (q0 + row < N) {
-            uint32_t a0, a1, a2, a3;
-            ld_shared_v4(stg + row * L::kDqRowBytes + 16 * c4, a0, a1, a2, a3);
-            red_add_v4(dq_acc + (size_t)(q0 + row) * D + half * DH + 4 * c4, __uint_as_float(a0),
-                       __uint_as_float(a1), __uint_as_float(a2), __uint_as_float(a3));
-          }
-        }
-      } else if constexpr (DQT) {
+      if constexpr (DQT) {
         // lane r holds dQ^T row r: column half*DH + r of query rows q0 .. q0+BM-1
         const int col = half * DH + r;
 #pragma unroll
@@ -636,11 +606,11 @@ cudaError_t launch_convert(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool DQB, bool BF16>
+template <int D, int DH, int BM, bool DQT, int STG, int NPB, bool BF16>
 cudaError_t launch_main(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                         const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BM, DQT, STG, NPB, DQB>;
-  auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, DQB, BF16>;
+  using L = BwdLayout<D, DH, BM, DQT, STG, NPB>;
+  auto kern = fa_bwd_kernel<D, DH, BM, DQT, STG, NPB, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc);
   if (e != cudaSuccess) return e;
   const long long nkb = (a.Nk + kBN - 1) / kBN;
@@ -673,10 +643,10 @@ cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
   switch (d) {
     case 64:
       return bf16 ? launch_all<64, true>(a, stream, [&] {
-        return launch_main<64, 64, 128, false, 3, 1, false, true>(q, k, v, dout, a, stream);
+        return launch_main<64, 64, 128, false, 3, 1, true>(q, k, v, dout, a, stream);
       })
                   : launch_all<64, false>(a, stream, [&] {
-                      return launch_main<64, 64, 128, false, 3, 1, false, false>(q, k, v, dout, a, stream);
+                      return launch_main<64, 64, 128, false, 3, 1, false>(q, k, v, dout, a, stream);
                     });
     case 128: {
       // No dQ accumulator: the dQ kernel writes dQ itself, so the pre-pass only
@@ -689,10 +659,10 @@ cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap
     }
     case 256:
       return bf16 ? launch_all<256, true>(a, stream, [&] {
-        return launch_main<256, 128, 64, true, 1, 1, false, true>(q, k, v, dout, a, stream);
+        return launch_main<256, 128, 64, true, 1, 1, true>(q, k, v, dout, a, stream);
       })
                   : launch_all<256, false>(a, stream, [&] {
-                      return launch_main<256, 128, 64, true, 1, 1, false, false>(q, k, v, dout, a, stream);
+                      return launch_main<256, 128, 64, true, 1, 1, false>(q, k, v, dout, a, stream);
                     });
     default:
       return cudaErrorInvalidValue;
