@@ -36,6 +36,7 @@ SIGNATURES = {
                        _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_check_device_status": (_i, [_vp]),
+    "fa_selftest_wait_timeout": (_i, [ctypes.c_uint32, _vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
     "fa_last_device_error_detail": (None, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
@@ -50,6 +51,7 @@ class FaError(RuntimeError):
         extra = f" (device record {detail})" if detail else ""
         super().__init__(f"{where} failed: {STATUS.get(code, code)}{extra}")
         self.code = code
+        self.detail = detail
 
 
 _lib = None
@@ -166,7 +168,13 @@ def fa_check_device_status(stream=None):
     if code != FA_OK:
         rec = (ctypes.c_uint32 * 4)()
         lib.fa_last_device_error_detail(rec)
-        raise FaError("fa_check_device_status", code, [hex(x) for x in rec])
+        raise FaError("fa_check_device_status", code, [int(x) for x in rec])
+
+
+def fa_selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch the failure-detection self-test (a wait that gives up after ``limit_us``);
+    the next fa_check_device_status reports it."""
+    _check("fa_selftest_wait_timeout", load().fa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def fa_profile_begin(n: int):

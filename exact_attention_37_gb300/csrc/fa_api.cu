@@ -327,6 +327,17 @@ fa_status fa_check_device_status(fa_stream_t stream) {
   return FA_OK;
 }
 
+fa_status fa_selftest_wait_timeout(uint32_t limit_us, fa_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return FA_ERR_INVALID_ARG;
+  fa_status st = check_device();
+  if (st != FA_OK) return st;
+  uint32_t* err = error_word_ptr();
+  if (!err) return FA_ERR_CUDA;
+  return launch_selftest_wait(err, 1000ull * limit_us, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 uint32_t fa_last_device_error_bits(void) { return g_last_detail[0]; }
 
 void fa_last_device_error_detail(uint32_t* out4) {

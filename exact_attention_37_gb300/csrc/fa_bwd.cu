@@ -1,6 +1,6 @@
 // Backward pass of exact attention for sm_103a: the pre-pass and dQ conversion
 // kernels, the launch sequence for every head dimension, and the fused main
-// kernel used for d = 64 and d = 256 (d = 128 runs the two deterministic main
+// kernel used for d = 256 (d = 64 and 128 run the two deterministic main
 // kernels of fa_bwd_sq.cu instead).
 //
 // The pages say the method serves training (page "FlashAttention-2 —
@@ -636,26 +636,21 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t stream, Main main) {
 
 int bwd_query_rows(int d) { return d == 256 ? 64 : 128; }
 
-bool bwd_needs_dq_acc(int d) { return d != 128; }
+bool bwd_needs_dq_acc(int d) { return d == 256; }
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
   switch (d) {
     case 64:
-      return bf16 ? launch_all<64, true>(a, stream, [&] {
-        return launch_main<64, 64, 128, false, 3, 1, true>(q, k, v, dout, a, stream);
-      })
-                  : launch_all<64, false>(a, stream, [&] {
-                      return launch_main<64, 64, 128, false, 3, 1, false>(q, k, v, dout, a, stream);
-                    });
     case 128: {
       // No dQ accumulator: the dQ kernel writes dQ itself, so the pre-pass only
       // computes D and L log2(e) and no conversion pass follows.
       BwdArgs a2 = a;
       a2.dq_acc = nullptr;
-      cudaError_t e = bf16 ? launch_pre<128, true>(a2, stream) : launch_pre<128, false>(a2, stream);
+      cudaError_t e = d == 64 ? (bf16 ? launch_pre<64, true>(a2, stream) : launch_pre<64, false>(a2, stream))
+                              : (bf16 ? launch_pre<128, true>(a2, stream) : launch_pre<128, false>(a2, stream));
       if (e != cudaSuccess) return e;
-      return launch_bwd_main_sq(bf16, q, k, v, dout, a2, stream);
+      return launch_bwd_main_sq(d, bf16, q, k, v, dout, a2, stream);
     }
     case 256:
       return bf16 ? launch_all<256, true>(a, stream, [&] {

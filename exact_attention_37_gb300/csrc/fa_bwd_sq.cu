@@ -1,4 +1,4 @@
-// Backward pass for head dimension 128 as two kernels on square 128 x 128 tiles,
+// Backward pass for head dimensions 64 and 128 as two kernels on 128 x 128 tiles,
 // with no atomics: every gradient element is summed in a fixed order inside one
 // CTA, so dQ, dK and dV are bitwise reproducible.
 //
@@ -35,9 +35,11 @@
 namespace fa {
 namespace {
 
-constexpr int kHd = 128;                  // head dimension
 constexpr uint32_t kPanel = 128 * 128;    // 128 rows x 128 B (64 16-bit columns)
-constexpr uint32_t kTile = 2 * kPanel;    // 128 rows x 128 columns
+// A 128-row tile of Q, K, V or dO with head dimension D: D / 64 panels.
+template <int D>
+constexpr uint32_t tile_bytes() { return (uint32_t)(D / 64) * kPanel; }
+constexpr uint32_t kSqTile = 2 * kPanel;  // a 128 x 128 16-bit tile (P^T)
 
 template <int NWG>
 struct SqCfg {
@@ -60,21 +62,23 @@ __device__ __forceinline__ void prefetch_l1(const void* p) {
 }
 
 constexpr uint32_t kIdSS(bool bf16) { return make_idesc_f16(bf16, 128, 128, false, false); }  // both K-major
-constexpr uint32_t kIdTS(bool bf16) { return make_idesc_f16(bf16, 128, 128, false, true); }   // A TMEM, B MN-major
+// N = D, A K-major (from TMEM or shared memory), B MN-major
+constexpr uint32_t kIdTS(bool bf16, int d) { return make_idesc_f16(bf16, 128, d, false, true); }
 constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand: 8-row groups 1024 B apart
 
-// D (128 x 128, fp32) = A B^T with A, B 128 x 128 K-major tiles in shared memory
-// (two 64-column panels each): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
+// Acc (128 x 128, fp32) = A B^T with A, B 128 x D K-major tiles in shared memory
+// (D / 64 panels each): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
+template <int D>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
   const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, 16);
 #pragma unroll
-  for (int kk = 0; kk < kHd / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
     mma_ss_lohi(d_tmem, a0 + off, kHi, b0 + off, kHi, idesc, kk > 0);
   }
 }
-// D (+)= A B with A (128 x 128) packed in TMEM by NWG warpgroups and B a 128 x 128
-// tile in shared memory read MN-major (rows = K, two 64-column panels of N).
+// Acc (+)= A B with A (128 x 128) packed in TMEM by NWG warpgroups and B a 128-row
+// tile in shared memory read MN-major (rows = K, 64-column panels of N).
 template <int NWG>
 __device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc,
                                            bool acc) {
@@ -85,7 +89,7 @@ __device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uin
                 (acc || kk > 0) ? 1u : 0u);
 }
 
-// D (+)= A B with A (128 x 128) a K-major tile in shared memory (rows = M, two
+// Acc (+)= A B with A (128 x 128) a K-major tile in shared memory (rows = M, two
 // 64-column panels of K) and B read MN-major as in mma_packed.
 __device__ __forceinline__ void mma_kmajor_a(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
                                              bool acc) {
@@ -95,6 +99,13 @@ __device__ __forceinline__ void mma_kmajor_a(uint32_t d_tmem, uint32_t a_smem, u
     const uint32_t a_off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
     mma_ss_lohi(d_tmem, a0 + a_off, kHi, b0 + ((kk * 2048) >> 4), kHi, idesc, (acc || kk > 0) ? 1u : 0u);
   }
+}
+
+// TMA load of one 128-row tile (D / 64 boxes of 64 columns) completing `bar`.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+#pragma unroll
+  for (int p = 0; p < D / 64; ++p) tma_load_3d(dst + p * kPanel, m, bar, 64 * p, row, plane);
 }
 
 // Stores 32 fp32 values (times mul) as 16-bit to dst (64 contiguous bytes).
@@ -110,12 +121,16 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&v)[3
 
 // ============================================================================ dK, dV
 namespace kv {
-constexpr uint32_t kSmK = 0;
-constexpr uint32_t kSmV = kTile;
-constexpr uint32_t kSmQ = 2 * kTile;   // two stages
-constexpr uint32_t kSmDO = 4 * kTile;  // two stages
-constexpr uint32_t kSmPt = 6 * kTile;  // P^T, 128 keys x 128 queries, K-major, two 64-query panels
-constexpr uint32_t kSmBar = 7 * kTile;
+template <int D>
+struct Smem {
+  static constexpr uint32_t T = tile_bytes<D>();
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = T;
+  static constexpr uint32_t kQ = 2 * T;    // two stages
+  static constexpr uint32_t kDO = 4 * T;   // two stages
+  static constexpr uint32_t kPt = 6 * T;   // P^T, 128 keys x 128 queries, K-major, two 64-query panels
+  static constexpr uint32_t kBar = 6 * T + kSqTile;
+};
 enum : int {
   kKVFull = 0,
   kQFull = 1,    // two
@@ -130,30 +145,35 @@ enum : int {
   kDone,         // the last dK product has completed
   kNumBars
 };
-constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
-constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;  // + alignment of the dynamic base
-static_assert(kSmAlloc <= 232448, "shared memory budget");
+template <int D>
+constexpr uint32_t tmem_slot() { return Smem<D>::kBar + kNumBars * 8; }
+template <int D>
+constexpr uint32_t smem_alloc() { return tmem_slot<D>() + 16 + 1024; }  // + alignment of the dynamic base
+static_assert(smem_alloc<128>() <= 232448, "shared memory budget");
 constexpr uint32_t kTmS = 0;     // S^T fp32
 constexpr uint32_t kTmDP = 128;  // dP^T fp32, then dS^T packed
 constexpr uint32_t kTmDV = 256;
-constexpr uint32_t kTmDK = 384;
+template <int D>
+constexpr uint32_t tm_dk() { return 256 + D; }
 }  // namespace kv
 
-template <int NWG, bool BF16>
+template <int D, int NWG, bool BF16>
 __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdArgs args) {
   using namespace kv;
   using C = SqCfg<NWG>;
+  using M = Smem<D>;
   constexpr int kCols = C::kCols, kCh = C::kCh;
+  constexpr uint32_t kTile = M::T, kSmTmemSlot = tmem_slot<D>(), kTmDK = tm_dk<D>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
-  auto sQ = [&](int s) -> uint32_t { return sbase + kSmQ + kTile * s; };
-  auto sDO = [&](int s) -> uint32_t { return sbase + kSmDO + kTile * s; };
-  const uint32_t sK = sbase + kSmK, sV = sbase + kSmV, sPt = sbase + kSmPt;
+  auto bar = [&](int i) -> uint32_t { return sbase + M::kBar + 8u * i; };
+  auto sQ = [&](int s) -> uint32_t { return sbase + M::kQ + kTile * s; };
+  auto sDO = [&](int s) -> uint32_t { return sbase + M::kDO + kTile * s; };
+  const uint32_t sK = sbase + M::kK, sV = sbase + M::kV, sPt = sbase + M::kPt;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -211,11 +231,8 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(bar(kKVFull), 2 * kTile);
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        tma_load_3d(sK + p * kPanel, &tm_k, bar(kKVFull), 64 * p, key0, bh_kv);
-        tma_load_3d(sV + p * kPanel, &tm_v, bar(kKVFull), 64 * p, key0, bh_kv);
-      }
+      load_tile<D>(sK, &tm_k, bar(kKVFull), key0, bh_kv);
+      load_tile<D>(sV, &tm_v, bar(kKVFull), key0, bh_kv);
       int n_do = 0, n_q = 0;  // loads issued
       for (int it = 0; it < nit; ++it) {
         const int s = it & 1, u = it >> 1;
@@ -223,13 +240,11 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         // Q first: S^T of a block is issued before its dP^T.
         if (u > 0 && !mbar_wait(bar(kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kQFull + s), kTile);
-        tma_load_3d(sQ(s), &tm_q, bar(kQFull + s), 0, q0, bq);
-        tma_load_3d(sQ(s) + kPanel, &tm_q, bar(kQFull + s), 64, q0, bq);
+        load_tile<D>(sQ(s), &tm_q, bar(kQFull + s), q0, bq);
         ++n_q;
         if (u > 0 && !mbar_wait(bar(kDOEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kDOFull + s), kTile);
-        tma_load_3d(sDO(s), &tm_do, bar(kDOFull + s), 0, q0, bq);
-        tma_load_3d(sDO(s) + kPanel, &tm_do, bar(kDOFull + s), 64, q0, bq);
+        load_tile<D>(sDO(s), &tm_do, bar(kDOFull + s), q0, bq);
         ++n_do;
       }
       // Every copy this thread issued lands before the CTA exits, even when the
@@ -251,13 +266,13 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       if (ok) ok = mbar_wait(bar(kQFull + 0), 0, args.err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + kTmS, sK, sQ(0), kIdSS(BF16));
+        mma_scores<D>(tmem + kTmS, sK, sQ(0), kIdSS(BF16));
         mma_commit(bar(kSReady));
         ok = mbar_wait(bar(kDOFull + 0), 0, args.err, kErrTimeoutTma);
       }
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + kTmDP, sV, sDO(0), kIdSS(BF16));
+        mma_scores<D>(tmem + kTmDP, sV, sDO(0), kIdSS(BF16));
         mma_commit(bar(kDpReady));
       }
       for (int it = 0; ok && it < nit; ++it) {
@@ -267,20 +282,20 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         if (it + 1 < nit) {
           if (!(ok = mbar_wait(bar(kQFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_scores(tmem + kTmS, sK, sQ(s1), kIdSS(BF16));
+          mma_scores<D>(tmem + kTmS, sK, sQ(s1), kIdSS(BF16));
           mma_commit(bar(kSReady));
         }
-        mma_kmajor_a(tmem + kTmDV, sPt, sDO(s), kIdTS(BF16), it > 0);
+        mma_kmajor_a(tmem + kTmDV, sPt, sDO(s), kIdTS(BF16, D), it > 0);
         mma_commit(bar(kPtFree));
         if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_packed<NWG>(tmem + kTmDK, tmem + kTmDP, sQ(s), kIdTS(BF16), it > 0);
+        mma_packed<NWG>(tmem + kTmDK, tmem + kTmDP, sQ(s), kIdTS(BF16, D), it > 0);
         mma_commit(bar(kQEmpty + s));   // Q(it): last read by dK(it)
         mma_commit(bar(kDOEmpty + s));  // dO(it): last read by dV(it)
         if (it + 1 < nit) {
           if (!(ok = mbar_wait(bar(kDOFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_scores(tmem + kTmDP, sV, sDO(s1), kIdSS(BF16));
+          mma_scores<D>(tmem + kTmDP, sV, sDO(s1), kIdSS(BF16));
           mma_commit(bar(kDpReady));
         } else {
           mma_commit(bar(kDone));
@@ -393,17 +408,18 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       warp_arrive(bar(kDsFull));
     }
     // ---- dV, dK of this key block once the last dK product has completed:
-    // lane r holds key row key0 + r, this warpgroup columns [kCols e, kCols (e + 1)).
+    // lane r holds key row key0 + r; the D / 32 column chunks go round-robin to the
+    // warpgroups.
     if (ok && warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma)) {
       tc_fence_after();
-      const size_t out_row = ((size_t)bh_kv * Nk + key) * kHd + cbeg;
+      const size_t out_row = ((size_t)bh_kv * Nk + key) * D;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = (which == 0 ? kTmDV : kTmDK) + cbeg;
+        const uint32_t col0 = which == 0 ? kTmDV : kTmDK;
         const float mul = which == 0 ? 1.f : args.scale;
         uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + out_row;
 #pragma unroll 1
-        for (int ch = 0; ch < kCh; ++ch) {
+        for (int ch = e; ch < D / 32; ch += NWG) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + lane_base + col0 + 32 * ch, v);
           tmem_wait_ld();
@@ -424,11 +440,15 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
 
 // ============================================================================ dQ
 namespace qk {
-constexpr uint32_t kSmQ = 0;
-constexpr uint32_t kSmDO = kTile;
-constexpr uint32_t kSmK = 2 * kTile;   // three stages (K is read by S and by dQ)
-constexpr uint32_t kSmV = 5 * kTile;   // two stages (V is read by dP only)
-constexpr uint32_t kSmBar = 7 * kTile;
+template <int D>
+struct Smem {
+  static constexpr uint32_t T = tile_bytes<D>();
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kDO = T;
+  static constexpr uint32_t kK = 2 * T;   // three stages (K is read by S and by dQ)
+  static constexpr uint32_t kV = 5 * T;   // two stages (V is read by dP only)
+  static constexpr uint32_t kBar = 7 * T;
+};
 enum : int {
   kQFull = 0,    // Q and dO
   kKFull = 1,    // three
@@ -442,29 +462,33 @@ enum : int {
   kDone = 17,    // the last dQ product has completed
   kNumBars
 };
-constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
-constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;
-static_assert(kSmAlloc <= 232448, "shared memory budget");
+template <int D>
+constexpr uint32_t tmem_slot() { return Smem<D>::kBar + kNumBars * 8; }
+template <int D>
+constexpr uint32_t smem_alloc() { return tmem_slot<D>() + 16 + 1024; }
+static_assert(smem_alloc<128>() <= 232448, "shared memory budget");
 constexpr uint32_t kTmS = 0;     // two buffers of 128: S fp32, then dS packed
 constexpr uint32_t kTmDP = 256;  // dP fp32
 constexpr uint32_t kTmDQ = 384;  // dQ accumulator
 }  // namespace qk
 
-template <int NWG, bool BF16>
+template <int D, int NWG, bool BF16>
 __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdArgs args) {
   using namespace qk;
   using C = SqCfg<NWG>;
+  using M = Smem<D>;
   constexpr int kCols = C::kCols, kCh = C::kCh;
+  constexpr uint32_t kTile = M::T, kSmTmemSlot = tmem_slot<D>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
-  auto sK = [&](int s) -> uint32_t { return sbase + kSmK + kTile * s; };
-  auto sV = [&](int s) -> uint32_t { return sbase + kSmV + kTile * s; };
-  const uint32_t sQ = sbase + kSmQ, sDO = sbase + kSmDO;
+  auto bar = [&](int i) -> uint32_t { return sbase + M::kBar + 8u * i; };
+  auto sK = [&](int s) -> uint32_t { return sbase + M::kK + kTile * s; };
+  auto sV = [&](int s) -> uint32_t { return sbase + M::kV + kTile * s; };
+  const uint32_t sQ = sbase + M::kQ, sDO = sbase + M::kDO;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -522,23 +546,18 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nkv > 0) {
       mbar_expect_tx(bar(kQFull), 2 * kTile);
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        tma_load_3d(sQ + p * kPanel, &tm_q, bar(kQFull), 64 * p, q0, bh);
-        tma_load_3d(sDO + p * kPanel, &tm_do, bar(kQFull), 64 * p, q0, bh);
-      }
+      load_tile<D>(sQ, &tm_q, bar(kQFull), q0, bh);
+      load_tile<D>(sDO, &tm_do, bar(kQFull), q0, bh);
       int n_k = 0, n_v = 0;  // loads issued
       for (int j = 0; j < nkv; ++j) {
         const int sk = j % 3, uk = j / 3, sv = j & 1, uv = j >> 1;
         if (uk > 0 && !mbar_wait(bar(kKEmpty + sk), (uk - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kKFull + sk), kTile);
-        tma_load_3d(sK(sk), &tm_k, bar(kKFull + sk), 0, 128 * j, bh_kv);
-        tma_load_3d(sK(sk) + kPanel, &tm_k, bar(kKFull + sk), 64, 128 * j, bh_kv);
+        load_tile<D>(sK(sk), &tm_k, bar(kKFull + sk), 128 * j, bh_kv);
         ++n_k;
         if (uv > 0 && !mbar_wait(bar(kVEmpty + sv), (uv - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kVFull + sv), kTile);
-        tma_load_3d(sV(sv), &tm_v, bar(kVFull + sv), 0, 128 * j, bh_kv);
-        tma_load_3d(sV(sv) + kPanel, &tm_v, bar(kVFull + sv), 64, 128 * j, bh_kv);
+        load_tile<D>(sV(sv), &tm_v, bar(kVFull + sv), 128 * j, bh_kv);
         ++n_v;
       }
       // Every copy this thread issued lands before the CTA exits.
@@ -559,20 +578,20 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       if (ok) ok = mbar_wait(bar(kKFull + 0), 0, args.err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + kTmS, sQ, sK(0), kIdSS(BF16));
+        mma_scores<D>(tmem + kTmS, sQ, sK(0), kIdSS(BF16));
         mma_commit(bar(kSReady + 0));
         ok = mbar_wait(bar(kVFull + 0), 0, args.err, kErrTimeoutTma);
       }
       if (ok) {
         tc_fence_after();
-        mma_scores(tmem + kTmDP, sDO, sV(0), kIdSS(BF16));
+        mma_scores<D>(tmem + kTmDP, sDO, sV(0), kIdSS(BF16));
         mma_commit(bar(kDpReady));
         mma_commit(bar(kVEmpty + 0));
         if (nkv > 1) {
           ok = mbar_wait(bar(kKFull + 1), 0, args.err, kErrTimeoutTma);
           if (ok) {
             tc_fence_after();
-            mma_scores(tmem + kTmS + 128, sQ, sK(1), kIdSS(BF16));
+            mma_scores<D>(tmem + kTmS + 128, sQ, sK(1), kIdSS(BF16));
             mma_commit(bar(kSReady + 1));
           }
         }
@@ -584,19 +603,19 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
           const int sv1 = (j + 1) & 1;
           if (!(ok = mbar_wait(bar(kVFull + sv1), ((j + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_scores(tmem + kTmDP, sDO, sV(sv1), kIdSS(BF16));
+          mma_scores<D>(tmem + kTmDP, sDO, sV(sv1), kIdSS(BF16));
           mma_commit(bar(kDpReady));
           mma_commit(bar(kVEmpty + sv1));
         }
         if (!(ok = mbar_wait(bar(kDsFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmS + 128 * b, sK(j % 3), kIdTS(BF16), j > 0);
+        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmS + 128 * b, sK(j % 3), kIdTS(BF16, D), j > 0);
         mma_commit(bar(kKEmpty + j % 3));  // K(j): last read by dQ(j)
         if (j + 2 < nkv) {
           const int sk2 = (j + 2) % 3;
           if (!(ok = mbar_wait(bar(kKFull + sk2), ((j + 2) / 3) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_scores(tmem + kTmS + 128 * b, sQ, sK(sk2), kIdSS(BF16));
+          mma_scores<D>(tmem + kTmS + 128 * b, sQ, sK(sk2), kIdSS(BF16));
           mma_commit(bar(kSReady + b));
         }
       }
@@ -668,15 +687,16 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       tc_fence_before();
       warp_arrive(bar(kDsFull + b));
     }
-    // ---- dQ rows: lane r holds query row q, this warpgroup columns [kCols e, kCols (e + 1)).
+    // ---- dQ rows: lane r holds query row q; the D / 32 column chunks go round-robin
+    // to the warpgroups.
     if (ok && (nkv == 0 || warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
       tc_fence_after();
-      uint16_t* dst = reinterpret_cast<uint16_t*>(args.dq) + ((size_t)bh * N + q) * kHd + cbeg;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(args.dq) + ((size_t)bh * N + q) * D;
 #pragma unroll 1
-      for (int ch = 0; ch < kCh; ++ch) {
+      for (int ch = e; ch < D / 32; ch += NWG) {
         uint32_t v[32];
         if (nkv > 0) {
-          tmem_ld_32x32b_x32(tmem + lane_base + kTmDQ + cbeg + 32 * ch, v);
+          tmem_ld_32x32b_x32(tmem + lane_base + kTmDQ + 32 * ch, v);
           tmem_wait_ld();
           reg_fence32(v);
         } else {
@@ -700,23 +720,24 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
 #define FA_BWD_SQ_NWG 4
 #endif
 
-template <bool BF16>
+template <int D, bool BF16>
 cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                       const BwdArgs& a, cudaStream_t stream) {
   constexpr int kNwg = FA_BWD_SQ_NWG;
   constexpr int kThreads = SqCfg<kNwg>::kThreads;
-  auto kkv = fa_bwd_kv_kernel<kNwg, BF16>;
-  auto kq = fa_bwd_q_kernel<kNwg, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv::kSmAlloc);
+  constexpr uint32_t kKvSmem = kv::smem_alloc<D>(), kQSmem = qk::smem_alloc<D>();
+  auto kkv = fa_bwd_kv_kernel<D, kNwg, BF16>;
+  auto kq = fa_bwd_q_kernel<D, kNwg, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kKvSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::kSmAlloc);
+  e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
   if (e != cudaSuccess) return e;
   const long long grid_kv = (long long)((a.Nk + 127) / 128) * a.BHkv;
   const long long grid_q = (long long)((a.N + 127) / 128) * a.BH;
   profile_mark_begin(stream);
-  kkv<<<(unsigned)grid_kv, kThreads, kv::kSmAlloc, stream>>>(q, k, v, dout, a);
+  kkv<<<(unsigned)grid_kv, kThreads, kKvSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kq<<<(unsigned)grid_q, kThreads, qk::kSmAlloc, stream>>>(q, k, v, dout, a);
+  kq<<<(unsigned)grid_q, kThreads, kQSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   profile_mark_end(stream, 1);
   return cudaSuccess;
@@ -724,9 +745,16 @@ cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensor
 
 }  // namespace
 
-cudaError_t launch_bwd_main_sq(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_bwd_main_sq(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
-  return bf16 ? launch_sq<true>(q, k, v, dout, a, stream) : launch_sq<false>(q, k, v, dout, a, stream);
+  switch (d) {
+    case 64:
+      return bf16 ? launch_sq<64, true>(q, k, v, dout, a, stream) : launch_sq<64, false>(q, k, v, dout, a, stream);
+    case 128:
+      return bf16 ? launch_sq<128, true>(q, k, v, dout, a, stream) : launch_sq<128, false>(q, k, v, dout, a, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fa

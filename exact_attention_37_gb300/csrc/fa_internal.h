@@ -69,9 +69,12 @@ size_t bwd_lse_offset(long long BH, int N, int d);
 size_t bwd_delta_offset(long long BH, int N, int d);
 inline int bwd_npad(int N) { return (N + 127) / 128 * 128; }
 
-// Main kernels of the backward pass with 128 x 128 tiles (d = 128): dK/dV, then dQ.
-cudaError_t launch_bwd_main_sq(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+// Main kernels of the backward pass with 128 x 128 tiles (d = 64, 128): dK/dV, then dQ.
+cudaError_t launch_bwd_main_sq(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
+
+// Failure-detection self-test: one bounded wait that nothing completes.
+cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);

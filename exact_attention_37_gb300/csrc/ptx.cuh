@@ -19,6 +19,7 @@ enum : uint32_t {
   kErrTimeoutSoftmax = 1u << 2,   // the MMA issuer never saw elementwise output
   kErrTimeoutRing = 1u << 3,      // the producer never got a free ring slot
   kErrTimeoutSync = 1u << 4,      // a warpgroup barrier never completed
+  kErrSelfTest = 1u << 5,         // the failure-detection self-test's wait (expected to give up)
   kErrAborted = 1u << 31,         // set with the first failure: every later wait gives up at once
 };
 
@@ -78,20 +79,25 @@ static __device__ __noinline__ void record_timeout(uint32_t* err, uint32_t code,
 
 // The final drain of a CTA's tensor-core work passes honor_abort = false: it
 // always waits (bounded) for the MMAs already issued before TMEM is released.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code,
-                                          bool honor_abort = true) {
+// `err` must point at the device error record.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                              bool honor_abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 63) == 63) {
       if (honor_abort && (*reinterpret_cast<volatile uint32_t*>(err) & kErrAborted)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         record_timeout(err, code, bar);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                          bool honor_abort = true) {
+  return mbar_wait_for(bar, parity, err, code, honor_abort, kWaitLimitNs);
 }
 
 // Warp-uniform bounded wait: every lane waits, and every lane sees a failure if

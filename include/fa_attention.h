@@ -91,12 +91,12 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
- * Bytes of device workspace `fa_bwd` needs: for d = 64 and d = 256 an fp32 dQ
- * accumulator [B,H,N,d] (those head dimensions sum dQ with reductions from
- * every key block), then two fp32 row vectors (L log2 e and D = rowsum(dO o O))
- * whose rows are padded per head to a multiple of 128, each part 256-byte
- * aligned.  Linear in N: about B*H*N*(4d + 8) bytes, or B*H*N*8 for d = 128,
- * whose dQ kernel keeps its accumulator on chip.
+ * Bytes of device workspace `fa_bwd` needs: for d = 256 an fp32 dQ accumulator
+ * [B,H,N,d] (that head dimension sums dQ with reductions from every key block),
+ * then two fp32 row vectors (L log2 e and D = rowsum(dO o O)) whose rows are
+ * padded per head to a multiple of 128, each part 256-byte aligned.  Linear in
+ * N: about B*H*N*(4d + 8) bytes for d = 256, B*H*N*8 for d = 64 and 128, whose
+ * dQ kernel keeps its accumulator on chip.
  * Returns 0 for invalid or empty sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -115,11 +115,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace    : device buffer of at least fa_bwd_workspace_size(B,H,N,d)
  *                  bytes, 256-byte aligned; contents need not be initialised
  *                  and are overwritten.
- * Launches, in order on `stream`: the pre-pass (D and L log2 e; for d = 64
- * and 256 it also zeroes the dQ accumulator), then for d = 128 a
+ * Launches, in order on `stream`: the pre-pass (D and L log2 e; for d = 256
+ * it also zeroes the dQ accumulator), then for d = 64 and 128 a
  * key-block-parallel dK/dV kernel and a query-block-parallel dQ kernel, for
- * d = 64 and 256 one key-block-parallel kernel (dK, dV, and dQ by fp32
- * reductions into the accumulator) and the dQ conversion.
+ * d = 256 one key-block-parallel kernel (dK, dV, and dQ by fp32 reductions into
+ * the accumulator) and the dQ conversion.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
@@ -133,10 +133,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * fa_bwd_workspace_size(B, H, N_q, d) bytes.  With B*H*N_q == 0 no query
  * row exists, so dk and dv are set to zero (cudaMemsetAsync on `stream`).
  * dK and dV are deterministic (one CTA sums each key row in a fixed order).
- * For d = 128 dQ is deterministic too (one CTA sums each query row over the
- * key blocks in a fixed order): repeated calls give bitwise equal gradients.
- * For d = 64 and 256 dQ accumulates fp32 reductions from every key block, so
- * its last bits depend on scheduling.
+ * For d = 64 and 128 dQ is deterministic too (one CTA sums each query row over
+ * the key blocks in a fixed order): repeated calls give bitwise equal
+ * gradients.  For d = 256 dQ accumulates fp32 reductions from every key block,
+ * so its last bits depend on scheduling.
  * fa_bwd(..., N, ...) is fa_bwd_ex with H_kv = H and N_q = N_k = N.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -157,8 +157,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * library's device memory, allocated when the library's device code is loaded
  * and held by every GPU that loads it until the process exits.  Calls whose
  * scratch would exceed 32 MiB (33554432 bytes) return FA_ERR_WORKSPACE and
- * launch nothing; with B*H = 1 that is N up to 127,100 rows at d = 64 and
- * 4,194,304 rows at d = 128.
+ * launch nothing; with B*H = 1 that is N up to 32,513 rows at d = 256 and
+ * 4,194,304 rows at d = 64 and 128.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.  No
@@ -180,13 +180,30 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  */
 fa_status fa_check_device_status(fa_stream_t stream);
 
+/*
+ * Failure-detection self-test (a diagnostic; the attention method has no
+ * counterpart): launches one thread that waits, through the same bounded wait
+ * every kernel of this library uses, on an mbarrier that nothing arrives on, with
+ * a limit of limit_us microseconds instead of the kernels' 4 s.  The wait gives
+ * up, records code 32 (self-test) in the device error record and the kernel
+ * returns; the next fa_check_device_status on `stream` returns
+ * FA_ERR_DEVICE_TIMEOUT with that record and clears it, and the context stays
+ * usable.  Returns FA_ERR_INVALID_ARG unless 0 < limit_us <= 1000000,
+ * FA_ERR_UNSUPPORTED on a device other than sm_103, FA_ERR_CUDA if the launch
+ * failed, FA_OK otherwise (asynchronous on `stream`).  Kernels of this library
+ * that run between the self-test and that status check see the failure bit and
+ * stop early, as after a real timeout.
+ */
+fa_status fa_selftest_wait_timeout(uint32_t limit_us, fa_stream_t stream);
+
 /* Raw device error word of the last fa_check_device_status (0 = none). */
 uint32_t fa_last_device_error_bits(void);
 
 /*
  * The error record behind it: out4[0] the bits, out4[1] the code of the first
  * wait that gave up (1 TMA tile, 2 tensor-core commit, 4 elementwise output,
- * 8 ring slot, 16 warpgroup barrier), out4[2] that CTA's index, out4[3] its
+ * 8 ring slot, 16 warpgroup barrier, 32 self-test), out4[2] that CTA's index,
+ * out4[3] its
  * barrier's shared-memory address.  After the first failure every other wait
  * of the grid gives up at once (bit 31), and kernels launched before the next
  * fa_check_device_status stop early: their results are not valid.
@@ -196,8 +213,10 @@ void fa_last_device_error_detail(uint32_t* out4);
 /*
  * Measurement hook.  fa_profile_begin(n) makes the next n calls of fa_fwd and
  * fa_bwd record a pair of CUDA events (created and owned by the library) on
- * their stream around their main kernel -- the fused forward kernel, or the
- * key-block backward kernel without its pre-pass and dQ conversion.
+ * their stream around their main kernels -- the fused forward kernel, or the
+ * backward main kernels (for d = 64 and 128 the dK/dV kernel and the dQ
+ * kernel, for d = 256 the key-block kernel) without the pre-pass and dQ
+ * conversion.
  * fa_profile_end waits for those events, writes each kernel's time in
  * milliseconds to out_ms[i] and its kind to out_kind[i] (0 forward, 1 backward),
  * in call order, stops recording and returns the number of entries written (at

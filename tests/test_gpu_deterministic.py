@@ -1,5 +1,6 @@
-"""Bitwise repeatability of the d = 128 backward pass (dK/dV kernel plus dQ
-kernel, no atomics): repeated calls on the same inputs give identical dQ, dK, dV.
+"""Bitwise repeatability of the d = 64 and d = 128 backward pass (dK/dV kernel
+plus dQ kernel, no atomics): repeated calls on the same inputs give identical
+dQ, dK, dV.
 """
 import pytest
 import torch
@@ -24,10 +25,12 @@ def built():
         Workload("det_mha", 2, 4, 1000, 128, "bf16", False, 1.0, (501, 502, 503, 504)),
         Workload("det_mha_causal", 2, 4, 1000, 128, "bf16", True, 1.0, (505, 506, 507, 508)),
         Workload("det_gqa_unequal", 1, 4, 700, 128, "fp16", True, 1.0, (509, 510, 511, 512), True, 2, 1000),
+        Workload("det_d64", 2, 3, 900, 64, "fp16", True, 1.0, (513, 514, 515, 516)),
+        Workload("det_d64_mqa", 1, 4, 500, 64, "bf16", False, 1.0, (517, 518, 519, 520), True, 1, 777),
     ],
     ids=lambda w: w.name,
 )
-def test_d128_backward_is_bitwise_repeatable(w):
+def test_backward_is_bitwise_repeatable(w):
     q, k, v, do = (x.cuda() for x in make_inputs(w, with_dout=True))
     o, lse = fa.forward(q, k, v, scale=w.scale, causal=w.causal)
     first = fa.backward(q, k, v, o, lse, do, scale=w.scale, causal=w.causal)

@@ -64,7 +64,7 @@ def test_noalloc_matches_workspace_backward_twice_in_a_row():
 def test_noalloc_rejects_sizes_over_its_scratch():
     lib = _lib.load()
     z = ctypes.c_void_p(16)
-    # d = 64 (fp32 dQ accumulator in the scratch) fits at most 127,100 rows in 32 MiB;
-    # one head of 127,101 rows must be refused.
-    code = lib.fa_bwd_noalloc(z, z, z, z, z, z, z, z, z, 1, 1, 127101, 64, ctypes.c_float(0.1), 0, 1, None)
+    # d = 256 (fp32 dQ accumulator in the scratch) fits at most 32,513 rows in 32 MiB;
+    # one head of 32,514 rows must be refused.
+    code = lib.fa_bwd_noalloc(z, z, z, z, z, z, z, z, z, 1, 1, 32514, 256, ctypes.c_float(0.1), 0, 1, None)
     assert code == 4  # FA_ERR_WORKSPACE
