@@ -273,6 +273,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--causal", type=int, choices=[0, 1], default=None, help="override the workload's mask")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward pass alone (default for forward-only workloads)")
+    ap.add_argument("--chunks", type=int, default=0, help="head chunks of the host-buffer (e2e) pipeline; 0 = library default")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -357,29 +358,37 @@ def main():
     flops_step = flops_fwd if fwd_only else attention_flops(w)
     value = world * flops_step * K / (total_ms / 1e3) / 1e12
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: fa_fwd_host / fa_fwd_bwd_host take
+    # pinned host tensors and pipeline head chunks (copies in, kernels, copies out) on the
+    # library's streams; the caller's stream waits for the whole step
     pin = lambda t: t.pin_memory()
     qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
     oh = torch.empty_like(q).pin_memory()
     lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    uploads = [(qh, qd), (kh, kd), (vh, vd)] + ([] if fwd_only else [(doh, dod)])
-    downloads = [(od, oh), (lse, lseh)]
+    host_in = [qh, kh, vh] + ([] if fwd_only else [doh])
+    host_out = [oh, lseh]
     if not fwd_only:
         dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v))
-        downloads += [(dq, dqh), (dk, dkh), (dv, dvh)]
-    h2d = sum(hx.numel() * hx.element_size() for hx, _ in uploads)
-    d2h = sum(hx.numel() * hx.element_size() for _, hx in downloads)
+        host_out += [dqh, dkh, dvh]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    scratch = torch.empty(fa.fa_host_scratch_size(B, H, N, d, not fwd_only), dtype=torch.uint8, device=dev)
+
+    def host_step():
+        if fwd_only:
+            fa.fa_fwd_host(qh, kh, vh, oh, lseh, scratch, w.scale, w.causal, args.chunks)
+        else:
+            fa.fa_fwd_bwd_host(qh, kh, vh, doh, oh, lseh, dqh, dkh, dvh, scratch, w.scale, w.causal, args.chunks)
+
+    for _ in range(2):
+        host_step()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     barrier(world)
     for i in range(K):
         flush.zero_()
         e2e_ev[i][0].record(stream)
-        for hsrc, dst in uploads:
-            dst.copy_(hsrc, non_blocking=True)
-        step()
-        for dsrc, hdst in downloads:
-            hdst.copy_(dsrc, non_blocking=True)
+        host_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -429,7 +438,10 @@ def main():
                 "main_kernel_frac_of_peak_sustained": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / peak},
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / K,
+                    "path": f"{'fa_fwd_host' if fwd_only else 'fa_fwd_bwd_host'} (C ABI, pinned host buffers, "
+                            f"{args.chunks if args.chunks > 0 else 'default'} head chunks)"},
             "gpu_launches": (1 if fwd_only else 4) * K,
             "clocks": clocks.summary(),
         }

@@ -26,13 +26,16 @@ from ._lib import (  # noqa: F401
     fa_bwd_workspace_size,
     fa_check_device_status,
     fa_fwd,
+    fa_fwd_bwd_host,
+    fa_fwd_host,
+    fa_host_scratch_size,
     fa_status_string,
     fa_version,
     load,
 )
 
 __all__ = ["forward", "backward", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_status",
-           "FaError", "load"]
+           "fa_fwd_host", "fa_fwd_bwd_host", "fa_host_scratch_size", "FaError", "load"]
 
 
 def _default_scale(d: int) -> float:

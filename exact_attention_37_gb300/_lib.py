@@ -35,6 +35,10 @@ SIGNATURES = {
     "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                        _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_host_scratch_size": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
+    "fa_fwd_bwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _i,
+                             _vp]),
     "fa_check_device_status": (_i, [_vp]),
     "fa_selftest_wait_timeout": (_i, [ctypes.c_uint32, _vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
@@ -159,6 +163,41 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool
     code = lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _stream(stream))
     _check("fa_bwd_noalloc", code)
+
+
+def fa_host_scratch_size(B: int, H: int, N: int, d: int, backward: bool = True) -> int:
+    return int(load().fa_host_scratch_size(B, H, N, d, int(bool(backward))))
+
+
+def _host_tensors(*ts):
+    for t in ts:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host entry points take contiguous CPU tensors (pinned for overlap)")
+
+
+def fa_fwd_host(q, k, v, o, lse, scratch, scale: float, causal: bool, chunks: int = 0, stream=None):
+    """Forward pass on host tensors (q, k, v, o [B,H,N,d]; lse [B,H,N] fp32) through a CUDA
+    ``scratch`` (uint8) of at least fa_host_scratch_size(B, H, N, d, False) bytes."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    _host_tensors(q, k, v, o, lse)
+    code = lib.fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(scratch),
+                           scratch.numel() * scratch.element_size(), B, H, N, d, float(scale), int(bool(causal)),
+                           _dtype_code(q), int(chunks), _stream(stream))
+    _check("fa_fwd_host", code)
+
+
+def fa_fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, scratch, scale: float, causal: bool, chunks: int = 0,
+                    stream=None):
+    """Forward and backward pass on host tensors through a CUDA ``scratch`` (uint8) of at
+    least fa_host_scratch_size(B, H, N, d, True) bytes; outputs valid after ``stream`` syncs."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    _host_tensors(q, k, v, dout, o, lse, dq, dk, dv)
+    code = lib.fa_fwd_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(scratch), scratch.numel() * scratch.element_size(), B, H, N, d,
+                               float(scale), int(bool(causal)), _dtype_code(q), int(chunks), _stream(stream))
+    _check("fa_fwd_bwd_host", code)
 
 
 def fa_check_device_status(stream=None):

@@ -181,6 +181,38 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 fa_status fa_check_device_status(fa_stream_t stream);
 
 /*
+ * Host-buffer entry points (a runtime convenience; the attention method has no
+ * counterpart): the forward pass, or the forward and backward pass, of a
+ * problem whose inputs and outputs live in host memory.  The B*H heads are split
+ * into `chunks` chunks of consecutive heads (chunks <= 0: min(B*H, 4); at most
+ * 64); chunk c's host-to-device copies, kernels and device-to-host copies run on
+ * three library-owned streams, so copies of one chunk overlap the kernels of
+ * another.  Every chunk is an independent problem (B = 1, H = heads of the
+ * chunk) computed by fa_fwd_ex / fa_bwd_ex, so the results equal those of the
+ * device entry points on the whole problem.
+ *   q,k,v,dout      : host inputs [B,H,N,d] (16-bit); dout only for fa_fwd_bwd_host
+ *   o,lse,dq,dk,dv  : host outputs, layouts as in fa_fwd / fa_bwd
+ *   dev_scratch     : device buffer of at least fa_host_scratch_size(B,H,N,d,bwd)
+ *                     bytes, 256-byte aligned, owned by the caller; it holds the
+ *                     device copies of every tensor and the backward workspace
+ * Multi-head attention with N_q = N_k = N only.  Host buffers should be pinned
+ * (page-locked); with pageable memory the copies are correct but do not overlap.
+ * The call is asynchronous: all work starts after the work already queued on
+ * `stream`, and `stream` waits for its completion, so the outputs are valid once
+ * `stream` has been synchronized.  Errors: as fa_fwd / fa_bwd, plus
+ * FA_ERR_WORKSPACE for a missing or small scratch; if a chunk fails part-way the
+ * call still makes `stream` wait for the copies already issued.  Calls from
+ * several host threads are serialized by the library.
+ */
+size_t fa_host_scratch_size(int B, int H, int N, int d, int with_backward);
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dev_scratch,
+                      size_t scratch_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                      int chunks, fa_stream_t stream);
+fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
+                          void* dq, void* dk, void* dv, void* dev_scratch, size_t scratch_bytes, int B, int H, int N,
+                          int d, float scale, int causal, fa_dtype dtype, int chunks, fa_stream_t stream);
+
+/*
  * Failure-detection self-test (a diagnostic; the attention method has no
  * counterpart): launches one thread that waits, through the same bounded wait
  * every kernel of this library uses, on an mbarrier that nothing arrives on, with

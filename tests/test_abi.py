@@ -143,3 +143,18 @@ def test_selftest_rejects_bad_limits_on_the_host(lib):
     # validated before any device work: 0 < limit_us <= 1 s
     assert lib.fa_selftest_wait_timeout(0, None) == 1
     assert lib.fa_selftest_wait_timeout(1000001, None) == 1
+
+
+def test_host_entry_points_validate_on_the_host(lib):
+    vp = ctypes.c_void_p
+    assert lib.fa_host_scratch_size(2, 3, 100, 128, 1) > lib.fa_host_scratch_size(2, 3, 100, 128, 0) > 0
+    assert lib.fa_host_scratch_size(1, 1, 8, 96, 1) == 0
+    assert lib.fa_host_scratch_size(0, 1, 8, 64, 1) == 0
+    p = vp(4096)
+    # empty problem: nothing to do
+    assert lib.fa_fwd_bwd_host(*([p] * 9), p, 1 << 20, 0, 2, 64, 64, 0.1, 0, 1, 0, None) == 0
+    # null input, missing scratch, small scratch, misaligned scratch: refused before any device work
+    assert lib.fa_fwd_bwd_host(*([vp(0)] + [p] * 8), p, 1 << 30, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 1
+    assert lib.fa_fwd_bwd_host(*([p] * 9), vp(0), 1 << 30, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 4
+    assert lib.fa_fwd_bwd_host(*([p] * 9), p, 100, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 4
+    assert lib.fa_fwd_host(*([p] * 5), vp(4096 + 16), 1 << 30, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 3
