@@ -450,15 +450,15 @@ struct Smem {
   static constexpr uint32_t kBar = 7 * T;
 };
 enum : int {
-  kQFull = 0,    // Q and dO
+  kQFull = 0,    // Q and dO tiles in shared memory
   kKFull = 1,    // three
   kKEmpty = 4,   // three
   kVFull = 7,    // two
   kVEmpty = 9,   // two
-  kSReady = 11,  // two: S of the block is in TMEM buffer b
-  kDpReady = 13, // dP of the block is in TMEM
-  kDpRead = 14,  // dP of the block has been read out of TMEM
-  kDsFull = 15,  // two, used alternately: dS of the block written into buffer b
+  kSReady = 11,  // S of the block is in TMEM
+  kPDone = 12,   // S read out
+  kDpReady = 13, // two, one per dP buffer: dP of the block is in the buffer
+  kDsFull = 15,  // two: dS written into the buffer's first columns
   kDone = 17,    // the last dQ product has completed
   kNumBars
 };
@@ -467,9 +467,11 @@ constexpr uint32_t tmem_slot() { return Smem<D>::kBar + kNumBars * 8; }
 template <int D>
 constexpr uint32_t smem_alloc() { return tmem_slot<D>() + 16 + 1024; }
 static_assert(smem_alloc<128>() <= 232448, "shared memory budget");
-constexpr uint32_t kTmS = 0;     // two buffers of 128: S fp32, then dS packed
-constexpr uint32_t kTmDP = 256;  // dP fp32
-constexpr uint32_t kTmDQ = 384;  // dQ accumulator
+// TMEM: S (fp32), two dP buffers (fp32, then dS packed into the first columns
+// of its buffer), and the dQ accumulator.
+constexpr uint32_t kTmS = 0;
+constexpr uint32_t kTmDP = 128;  // buffer b at 128 + 128 b
+constexpr uint32_t kTmDQ = 384;
 }  // namespace qk
 
 template <int D, int NWG, bool BF16>
@@ -518,12 +520,13 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
-      mbar_init(bar(kSReady + s), 1);
     }
-    mbar_init(bar(kDpReady), 1);
-    mbar_init(bar(kDpRead), C::kEw / 32);  // one arrival per elementwise warp
-    mbar_init(bar(kDsFull + 0), C::kEw / 32);
-    mbar_init(bar(kDsFull + 1), C::kEw / 32);
+    mbar_init(bar(kSReady), 1);
+    mbar_init(bar(kPDone), C::kEw / 32);  // one arrival per elementwise warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kDpReady + b), 1);
+      mbar_init(bar(kDsFull + b), C::kEw / 32);
+    }
     mbar_init(bar(kDone), 1);
     fence_mbar_init();
   }
@@ -569,55 +572,40 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     }
   } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Order: S(0) dP(0) S(1) | dP(j+1) dQ(j) S(j+2) | ...  dP(j+1) overwrites dP(j)
-    // as soon as the elementwise warps have read it out (DpRead), while they still
-    // compute dS(j); S(j+2) overwrites dS(j) in buffer j % 2 only after dQ(j) has
-    // read it (issue order).
+    // Order: S(0) dP(0) dP(1) | S(j+1) dQ(j) dP(j+2) | ...  S(j+1) follows as soon as
+    // S(j) has been read out; dP(j+2) goes into the buffer of block j, whose dS(j)
+    // dQ(j) has just read (one thread's tcgen05.mma operations execute in issue
+    // order), so dP runs two blocks ahead of the elementwise warps.
     if (lane == 0 && nkv > 0) {
+      constexpr uint32_t kIdG = kIdTS(BF16, D);
+      auto issue_s = [&](int j) -> bool {
+        if (!mbar_wait(bar(kKFull + j % 3), (j / 3) & 1, args.err, kErrTimeoutTma)) return false;
+        tc_fence_after();
+        mma_scores<D>(tmem + kTmS, sQ, sK(j % 3), kIdSS(BF16));
+        mma_commit(bar(kSReady));
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {
+        if (!mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, args.err, kErrTimeoutTma)) return false;
+        tc_fence_after();
+        mma_scores<D>(tmem + kTmDP + 128 * (j & 1), sDO, sV(j & 1), kIdSS(BF16));
+        mma_commit(bar(kDpReady + (j & 1)));
+        mma_commit(bar(kVEmpty + (j & 1)));
+        return true;
+      };
       bool ok = mbar_wait(bar(kQFull), 0, args.err, kErrTimeoutTma);
-      if (ok) ok = mbar_wait(bar(kKFull + 0), 0, args.err, kErrTimeoutTma);
-      if (ok) {
-        tc_fence_after();
-        mma_scores<D>(tmem + kTmS, sQ, sK(0), kIdSS(BF16));
-        mma_commit(bar(kSReady + 0));
-        ok = mbar_wait(bar(kVFull + 0), 0, args.err, kErrTimeoutTma);
-      }
-      if (ok) {
-        tc_fence_after();
-        mma_scores<D>(tmem + kTmDP, sDO, sV(0), kIdSS(BF16));
-        mma_commit(bar(kDpReady));
-        mma_commit(bar(kVEmpty + 0));
-        if (nkv > 1) {
-          ok = mbar_wait(bar(kKFull + 1), 0, args.err, kErrTimeoutTma);
-          if (ok) {
-            tc_fence_after();
-            mma_scores<D>(tmem + kTmS + 128, sQ, sK(1), kIdSS(BF16));
-            mma_commit(bar(kSReady + 1));
-          }
-        }
-      }
+      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_dp(0);
+      if (ok && nkv > 1) ok = issue_dp(1);
       for (int j = 0; ok && j < nkv; ++j) {
         const int b = j & 1;
-        if (!(ok = mbar_wait(bar(kDpRead), j & 1, args.err, kErrTimeoutSoftmax))) break;
-        if (j + 1 < nkv) {
-          const int sv1 = (j + 1) & 1;
-          if (!(ok = mbar_wait(bar(kVFull + sv1), ((j + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
-          tc_fence_after();
-          mma_scores<D>(tmem + kTmDP, sDO, sV(sv1), kIdSS(BF16));
-          mma_commit(bar(kDpReady));
-          mma_commit(bar(kVEmpty + sv1));
-        }
+        if (!(ok = mbar_wait(bar(kPDone), j & 1, args.err, kErrTimeoutSoftmax))) break;
+        if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
         if (!(ok = mbar_wait(bar(kDsFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmS + 128 * b, sK(j % 3), kIdTS(BF16, D), j > 0);
+        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmDP + 128 * b, sK(j % 3), kIdG, j > 0);
         mma_commit(bar(kKEmpty + j % 3));  // K(j): last read by dQ(j)
-        if (j + 2 < nkv) {
-          const int sk2 = (j + 2) % 3;
-          if (!(ok = mbar_wait(bar(kKFull + sk2), ((j + 2) / 3) & 1, args.err, kErrTimeoutTma))) break;
-          tc_fence_after();
-          mma_scores<D>(tmem + kTmS + 128 * b, sQ, sK(sk2), kIdSS(BF16));
-          mma_commit(bar(kSReady + b));
-        }
+        if (j + 2 < nkv && !(ok = issue_dp(j + 2))) break;
       }
       mma_commit(bar(kDone));
       mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
@@ -632,19 +620,18 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     const float c = args.scale_log2;
     const float Lr = args.lse_log2[(size_t)bh * args.Npad + q];  // +inf on padding rows: P = 0
     const float Dr = args.delta[(size_t)bh * args.Npad + q];
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int b = j & 1;
+    bool ok = nkv > 0;
+    for (int j = 0; ok && j < nkv; ++j) {
       const int k0 = 128 * j;
       const bool diag = args.causal && (k0 + 127 > q0 + koff);  // some key hidden from some query
       // ---- P = 2^(S c - L log2 e), kept in registers
-      if (!(ok = warp_wait(bar(kSReady + b), (j >> 1) & 1, args.err, kErrTimeoutMma))) break;
+      if (!(ok = warp_wait(bar(kSReady), j & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
       float p[kCols];
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         uint32_t sv[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 128 * b + cbeg + 32 * ch, sv);
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cbeg + 32 * ch, sv);
         tmem_wait_ld();
         reg_fence32(sv);
 #pragma unroll
@@ -660,28 +647,29 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
             if (k0 + cbeg + 32 * ch + x > q + koff) p[32 * ch + x] = 0.f;
         }
       }
-      // ---- dS = P o (dP - D), packed into the S columns of buffer b
-      if (!(ok = warp_wait(bar(kDpReady), j & 1, args.err, kErrTimeoutMma))) break;
-      tc_fence_after();
-      uint32_t dv[kCh][32];
-#pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv[ch]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) reg_fence32(dv[ch]);
       tc_fence_before();
-      warp_arrive(bar(kDpRead));  // the next dP may overwrite these columns now
+      warp_arrive(bar(kPDone));  // S may be overwritten by the next block's scores now
+      // ---- dS = P o (dP - D), packed into the first columns of this warpgroup's part
+      // of the block's dP buffer
+      const int b = j & 1;
+      const uint32_t dpb = tmem + lane_base + kTmDP + 128 * b + cbeg;
+      if (!(ok = warp_wait(bar(kDpReady + b), (j >> 1) & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(dpb + 32 * ch, dv);
+        tmem_wait_ld();
+        reg_fence32(dv);
         uint32_t dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
           float ds0, ds1;
-          submul2(p[32 * ch + x], p[32 * ch + x + 1], __uint_as_float(dv[ch][x]), __uint_as_float(dv[ch][x + 1]), Dr,
-                  Dr, ds0, ds1);
+          submul2(p[32 * ch + x], p[32 * ch + x + 1], __uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), Dr, Dr,
+                  ds0, ds1);
           dw[x >> 1] = pack2<BF16>(ds0, ds1);
         }
-        tmem_st_32x32b_x16(tmem + lane_base + kTmS + 128 * b + cbeg + 16 * ch, dw);
+        tmem_st_32x32b_x16(dpb + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -689,7 +677,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     }
     // ---- dQ rows: lane r holds query row q; the D / 32 column chunks go round-robin
     // to the warpgroups.
-    if (ok && (nkv == 0 || warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
+    if (nkv == 0 || (ok && warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
       tc_fence_after();
       uint16_t* dst = reinterpret_cast<uint16_t*>(args.dq) + ((size_t)bh * N + q) * D;
 #pragma unroll 1
