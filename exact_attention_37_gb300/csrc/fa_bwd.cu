@@ -102,10 +102,6 @@ struct BwdLayout {
   static_assert(DQT || BM == 128, "dQ needs M = 128");
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 __device__ __forceinline__ void red_add(float* addr, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
@@ -515,54 +511,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // D_i = sum_c dO_ic O_ic per row, L_i * log2(e) copied next to it, and the fp32
 // dQ accumulator set to zero.  Both row vectors are padded per head to Npad rows
 // (a multiple of 128) so the main kernels read whole aligned blocks; padding rows
-// get L = +inf (P = 0) and D = 0.  One warp per padded row, grid-stride; each lane
-// handles D/32 consecutive elements.
+// get L = +inf (P = 0) and D = 0.  D / 8 lanes share a row, each loading 16 bytes
+// of O and of dO, so a warp covers 256 / D rows per step; two steps are in flight
+// per iteration to keep enough loads outstanding for the memory system.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs args, long long slots) {
-  constexpr int kPer = D / 32;  // 2, 4 or 8 elements per lane
+  constexpr int kLpr = D / 8;            // lanes per row
+  constexpr int kRpw = 32 / kLpr;        // rows per warp step
   const int lane = threadIdx.x & 31;
+  const int sub = lane / kLpr, part = lane % kLpr;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const uint16_t* o = reinterpret_cast<const uint16_t*>(args.o);
   const uint16_t* g = reinterpret_cast<const uint16_t*>(args.dout);
-  for (long long slot = warp0; slot < slots; slot += nwarps) {
-    const long long head = slot / args.Npad;
-    const int i = (int)(slot - head * args.Npad);
-    if (i >= args.N) {
-      if (lane == 0) {
-        args.lse_log2[slot] = INFINITY;
-        args.delta[slot] = 0.f;
+  const long long steps = (slots + kRpw - 1) / kRpw;
+  for (long long st0 = warp0; st0 < steps; st0 += 2 * nwarps) {
+    uint4 ov[2], gv[2];
+    long long slot[2], row[2];
+    bool valid[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const long long st = st0 + k * nwarps;
+      slot[k] = st * kRpw + sub;
+      const long long head = slot[k] / args.Npad;
+      const int i = (int)(slot[k] - head * args.Npad);
+      valid[k] = st < steps && slot[k] < slots && i < args.N;
+      row[k] = head * args.N + i;
+      if (valid[k]) {
+        const size_t base = (size_t)row[k] * D + part * 8;
+        ov[k] = *reinterpret_cast<const uint4*>(o + base);
+        gv[k] = *reinterpret_cast<const uint4*>(g + base);
+      } else {
+        ov[k] = make_uint4(0, 0, 0, 0);
+        gv[k] = make_uint4(0, 0, 0, 0);
       }
-      continue;
-    }
-    const long long row = head * args.N + i;
-    const size_t base = (size_t)row * D + lane * kPer;
-    float acc = 0.f;
-    uint16_t ov[kPer], gv[kPer];
-    if constexpr (kPer == 8) {
-      *reinterpret_cast<uint4*>(ov) = *reinterpret_cast<const uint4*>(o + base);
-      *reinterpret_cast<uint4*>(gv) = *reinterpret_cast<const uint4*>(g + base);
-    } else if constexpr (kPer == 4) {
-      *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(o + base);
-      *reinterpret_cast<uint2*>(gv) = *reinterpret_cast<const uint2*>(g + base);
-    } else {
-      *reinterpret_cast<uint32_t*>(ov) = *reinterpret_cast<const uint32_t*>(o + base);
-      *reinterpret_cast<uint32_t*>(gv) = *reinterpret_cast<const uint32_t*>(g + base);
     }
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      acc = fmaf(widen16<BF16>(ov[e]), widen16<BF16>(gv[e]), acc);
-    }
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+      const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+      float acc = 0.f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      args.delta[slot] = acc;
-      args.lse_log2[slot] = args.lse[row] * kLog2e;
-    }
-    if (args.dq_acc) {
-      float* z = args.dq_acc + base;
+      for (int w = 0; w < 4; ++w) {
+        acc = fmaf(widen16<BF16>((uint16_t)(ow[w] & 0xFFFFu)), widen16<BF16>((uint16_t)(gw[w] & 0xFFFFu)), acc);
+        acc = fmaf(widen16<BF16>((uint16_t)(ow[w] >> 16)), widen16<BF16>((uint16_t)(gw[w] >> 16)), acc);
+      }
 #pragma unroll
-      for (int e = 0; e < kPer; e += 2) *reinterpret_cast<float2*>(z + e) = make_float2(0.f, 0.f);
+      for (int off = kLpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (st0 + k * nwarps < steps && slot[k] < slots && part == 0) {
+        if (valid[k]) {
+          args.delta[slot[k]] = acc;
+          args.lse_log2[slot[k]] = args.lse[row[k]] * kLog2e;
+        } else {
+          args.lse_log2[slot[k]] = INFINITY;  // padding row
+          args.delta[slot[k]] = 0.f;
+        }
+      }
+      if (args.dq_acc && valid[k]) {
+        float4* z = reinterpret_cast<float4*>(args.dq_acc + (size_t)row[k] * D + part * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -591,8 +600,8 @@ int num_sms() {
 template <int D, bool BF16>
 cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long slots = (long long)a.BH * a.Npad;
-  const long long want = (slots + 7) / 8;
-  const int grid = (int)std::min<long long>(want, (long long)num_sms() * 16);
+  const long long want = (slots * D / 256 + 7) / 8;  // warp steps / warps per block
+  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms() * 16));
   fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(a, slots);
   return cudaGetLastError();
 }
