@@ -33,9 +33,10 @@
 // Warp roles: warps 0-7 (two warpgroups, half of the query columns each) turn
 // S^T and dP^T into P^T and dS^T, releasing the S^T/dP^T accumulators as soon
 // as they have read them so the next block's scores overlap this block's
-// exponentials; warps 8-11 drain dQ from TMEM into the fp32 accumulator and
-// write dK, dV at the end; warp 12 issues TMA loads; warp 13 issues the tcgen05
-// MMAs.
+// exponentials; warps 8-11 drain dQ from TMEM into the fp32 accumulator (lane =
+// head-dimension index: each reduction instruction covers 32 consecutive columns
+// of one query row) and write dK, dV at the end; warp 12 issues TMA loads; warp 13
+// issues the tcgen05 MMAs.
 #include <algorithm>
 
 #include "fa_internal.h"

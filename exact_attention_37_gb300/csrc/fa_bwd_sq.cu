@@ -13,20 +13,24 @@
 // fa_bwd_kv_kernel: one CTA per (key/value head, 128-key block), looping over the
 //   query blocks of every query head of the group (the key-block parallelism of
 //   page "FlashAttention-2 — فلاش أتنشن-2", section "Technical architecture",
-//   item 2).  Keys sit on TMEM lanes: S^T = K Q^T, dP^T = V dO^T; P^T and dS^T are
-//   written back as packed 16-bit pairs into the columns their fp32 sources came
-//   from and feed dV += P^T dO and dK += dS^T Q as tensor-memory A operands.
+//   item 2).  Keys sit on TMEM lanes: S^T = K Q^T, dP^T = V dO^T.  P^T goes to
+//   shared memory (K-major) and feeds dV += P^T dO, so the next block's S^T can
+//   start as soon as S^T has been read out; dS^T is written back as packed 16-bit
+//   pairs into the columns of dP^T and feeds dK += dS^T Q as the tensor-memory A
+//   operand.
 // fa_bwd_q_kernel: one CTA per (query head, 128-row query block), looping over the
-//   key blocks its rows see.  Queries sit on TMEM lanes: S = Q K^T, dP = dO V^T;
-//   dS goes back into the S columns as packed pairs and feeds dQ += dS K; dQ stays
-//   in TMEM until the CTA writes it once, scaled and rounded.
+//   key blocks its rows see.  Queries sit on TMEM lanes: S = Q K^T and dP = dO V^T
+//   (two dP buffers, so dP runs two key blocks ahead); dS goes back into its dP
+//   buffer as packed pairs and feeds dQ += dS K; dQ stays in TMEM until the CTA
+//   writes it once, scaled and rounded.
 //
 // The second kernel recomputes S and dP (7 products per tile pair instead of 5);
 // in exchange no fp32 reductions leave the SM, and the dQ accumulator, its
 // zeroing and its conversion pass disappear.
 //
-// Every product has M = N = 128.  Warps: 4 NWG elementwise warps (NWG warpgroups,
-// 128 / NWG tile columns each), one TMA warp, one MMA warp.
+// The score products have M = N = 128, the gradient products N = d.  Warps: 4 NWG
+// elementwise warps (NWG warpgroups, 128 / NWG tile columns each; every warp
+// arrives once on the barriers it signals), one TMA warp, one MMA warp.
 #include <algorithm>
 
 #include "fa_internal.h"
