@@ -35,8 +35,9 @@ def test_grouped_query_forward_and_backward(H_kv, causal, d):
 
 @pytest.mark.parametrize("N,N_k", [(100, 300), (300, 100), (1, 257), (257, 1), (129, 640), (640, 129)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_unequal_lengths_forward_and_backward(N, N_k, causal):
-    w = w_ex(2, 1, N, N_k, 128, "fp16", causal)
+@pytest.mark.parametrize("d", [64, 128])
+def test_unequal_lengths_forward_and_backward(N, N_k, causal, d):
+    w = w_ex(2, 1, N, N_k, d, "fp16", causal)
     parity.check_forward_full(w)
     parity.check_backward_full(w)
 

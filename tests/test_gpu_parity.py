@@ -112,6 +112,13 @@ def test_ctx32k_workload_forward_sampled():
     parity.check_forward_sampled(w, synth.sample_heads(w), synth.sample_rows(w.N, 64))
 
 
+def test_ctx32k_backward_one_head():
+    # the longest sequence of the workloads (N = 32768), backward included: two heads
+    # on the GPU, the second checked in full against the oracle (row chunks)
+    w = synth.CTX32K.with_(H=2, backward=True)
+    parity.check_backward_sampled(w, [(0, 1)])
+
+
 def test_forward_allocates_nothing_beyond_its_outputs():
     """O(N) memory: at N = 32768 a single fp32 score matrix of one head would take
     4.3 GB; the forward call's footprint is its two outputs (allocated by torch in
