@@ -403,7 +403,7 @@ def main():
     flops_bwd = attention_flops(w) - flops_fwd
     if bwd_main_avg >= fwd_avg:
         # the main backward launches between the library's marks: dK/dV + dQ kernels
-        # for d = 128, the fused kernel otherwise
+        # for d = 64 and 128, the fused kernel for d = 256
         dom, dom_ms, dom_flops = "fa_bwd_main", bwd_main_avg, flops_bwd
     else:
         dom, dom_ms, dom_flops = "fa_fwd_kernel", fwd_avg, flops_fwd
