@@ -13,11 +13,11 @@
 // fa_bwd_kv_kernel: one CTA per (key/value head, 128-key block), looping over the
 //   query blocks of every query head of the group (the key-block parallelism of
 //   page "FlashAttention-2 — فلاش أتنشن-2", section "Technical architecture",
-//   item 2).  Keys sit on TMEM lanes: S^T = K Q^T, dP^T = V dO^T.  P^T goes to
-//   shared memory (K-major) and feeds dV += P^T dO, so the next block's S^T can
-//   start as soon as S^T has been read out; dS^T is written back as packed 16-bit
-//   pairs into the columns of dP^T and feeds dK += dS^T Q as the tensor-memory A
-//   operand.
+//   item 2).  Keys sit on TMEM lanes: S^T = K Q^T, dP^T = V dO^T.  P^T is written
+//   back as packed 16-bit pairs into the columns of S^T and feeds dV += P^T dO as
+//   the tensor-memory A operand; dS^T likewise goes into the columns of dP^T and
+//   feeds dK += dS^T Q.  Only the B operands (dO, Q) are read from shared memory
+//   by the gradient products.
 // fa_bwd_q_kernel: one CTA per (query head, 128-row query block), looping over the
 //   key blocks its rows see.  Queries sit on TMEM lanes: S = Q K^T and dP = dO V^T
 //   (two dP buffers, so dP runs two key blocks ahead); dS goes back into its dP
@@ -43,7 +43,6 @@ constexpr uint32_t kPanel = 128 * 128;    // 128 rows x 128 B (64 16-bit columns
 // A 128-row tile of Q, K, V or dO with head dimension D: D / 64 panels.
 template <int D>
 constexpr uint32_t tile_bytes() { return (uint32_t)(D / 64) * kPanel; }
-constexpr uint32_t kSqTile = 2 * kPanel;  // a 128 x 128 16-bit tile (P^T)
 
 template <int NWG>
 struct SqCfg {
@@ -61,8 +60,8 @@ struct SqCfg {
 __device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+__device__ __forceinline__ void ld_shared_f4(uint32_t addr, float4& v) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
 }
 
 constexpr uint32_t kIdSS(bool bf16) { return make_idesc_f16(bf16, 128, 128, false, false); }  // both K-major
@@ -93,18 +92,6 @@ __device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uin
                 (acc || kk > 0) ? 1u : 0u);
 }
 
-// Acc (+)= A B with A (128 x 128) a K-major tile in shared memory (rows = M, two
-// 64-column panels of K) and B read MN-major as in mma_packed.
-__device__ __forceinline__ void mma_kmajor_a(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
-                                             bool acc) {
-  const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, kPanel);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t a_off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
-    mma_ss_lohi(d_tmem, a0 + a_off, kHi, b0 + ((kk * 2048) >> 4), kHi, idesc, (acc || kk > 0) ? 1u : 0u);
-  }
-}
-
 // TMA load of one 128-row tile (D / 64 boxes of 64 columns) completing `bar`.
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
@@ -132,8 +119,8 @@ struct Smem {
   static constexpr uint32_t kV = T;
   static constexpr uint32_t kQ = 2 * T;    // two stages
   static constexpr uint32_t kDO = 4 * T;   // two stages
-  static constexpr uint32_t kPt = 6 * T;   // P^T, 128 keys x 128 queries, K-major, two 64-query panels
-  static constexpr uint32_t kBar = 6 * T + kSqTile;
+  static constexpr uint32_t kLD = 6 * T;   // two stages of L log2 e (512 B) and D (512 B) of a query block
+  static constexpr uint32_t kBar = 6 * T + 2048;
 };
 enum : int {
   kKVFull = 0,
@@ -142,8 +129,7 @@ enum : int {
   kDOFull = 5,   // two
   kDOEmpty = 7,  // two
   kSReady = 9,   // S^T of the block is in TMEM
-  kPFull,        // S^T read out and P^T written to shared memory
-  kPtFree,       // dV has read P^T
+  kPFull,        // S^T read out and P^T written back packed into its columns
   kDpReady,      // dP^T of the block is in TMEM
   kDsFull,       // dS^T written
   kDone,         // the last dK product has completed
@@ -154,7 +140,7 @@ constexpr uint32_t tmem_slot() { return Smem<D>::kBar + kNumBars * 8; }
 template <int D>
 constexpr uint32_t smem_alloc() { return tmem_slot<D>() + 16 + 1024; }  // + alignment of the dynamic base
 static_assert(smem_alloc<128>() <= 232448, "shared memory budget");
-constexpr uint32_t kTmS = 0;     // S^T fp32
+constexpr uint32_t kTmS = 0;     // S^T fp32, then P^T packed
 constexpr uint32_t kTmDP = 128;  // dP^T fp32, then dS^T packed
 constexpr uint32_t kTmDV = 256;
 template <int D>
@@ -177,7 +163,8 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + M::kBar + 8u * i; };
   auto sQ = [&](int s) -> uint32_t { return sbase + M::kQ + kTile * s; };
   auto sDO = [&](int s) -> uint32_t { return sbase + M::kDO + kTile * s; };
-  const uint32_t sK = sbase + M::kK, sV = sbase + M::kV, sPt = sbase + M::kPt;
+  const uint32_t sK = sbase + M::kK, sV = sbase + M::kV;
+  auto sLD = [&](int s) -> uint32_t { return sbase + M::kLD + 1024u * s; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,7 +197,6 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     }
     mbar_init(bar(kSReady), 1);
     mbar_init(bar(kPFull), C::kEw / 32);  // one arrival per elementwise warp
-    mbar_init(bar(kPtFree), 1);
     mbar_init(bar(kDpReady), 1);
     mbar_init(bar(kDsFull), C::kEw / 32);
     mbar_init(bar(kDone), 1);
@@ -243,8 +229,10 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         const int q0 = q_block(it) * 128, bq = q_head(it);
         // Q first: S^T of a block is issued before its dP^T.
         if (u > 0 && !mbar_wait(bar(kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
-        mbar_expect_tx(bar(kQFull + s), kTile);
+        mbar_expect_tx(bar(kQFull + s), kTile + 1024);
         load_tile<D>(sQ(s), &tm_q, bar(kQFull + s), q0, bq);
+        bulk_load(sLD(s), args.lse_log2 + (size_t)bq * args.Npad + q0, 512, bar(kQFull + s));
+        bulk_load(sLD(s) + 512, args.delta + (size_t)bq * args.Npad + q0, 512, bar(kQFull + s));
         ++n_q;
         if (u > 0 && !mbar_wait(bar(kDOEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kDOFull + s), kTile);
@@ -261,10 +249,11 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     }
   } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Order: S(0) dP(0) | S(i+1) dV(i) dK(i) dP(i+1) | ...  S(i+1) follows as soon
-    // as S^T(i) has been read out (P^T(i) is in shared memory); dP(i+1) overwrites
-    // dS^T(i) only after dK(i) has read it, because one thread's tcgen05.mma
-    // operations execute in issue order.
+    // Order: S(0) dP(0) | dV(i) S(i+1) dK(i) dP(i+1) | ...  S(i+1) overwrites the
+    // packed P^T(i) only after dV(i) has read it, and dP(i+1) overwrites dS^T(i)
+    // only after dK(i) has read it, because one thread's tcgen05.mma operations
+    // execute in issue order.  dO(i) is free once dV(i) completes, Q(i) once dK(i)
+    // completes.
     if (lane == 0) {
       bool ok = mbar_wait(bar(kKVFull), 0, args.err, kErrTimeoutTma);
       if (ok) ok = mbar_wait(bar(kQFull + 0), 0, args.err, kErrTimeoutTma);
@@ -283,19 +272,18 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         const int s = it & 1, s1 = (it + 1) & 1;
         if (!(ok = mbar_wait(bar(kPFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
+        mma_packed<NWG>(tmem + kTmDV, tmem + kTmS, sDO(s), kIdTS(BF16, D), it > 0);
+        mma_commit(bar(kDOEmpty + s));  // dO(it): last read by dV(it)
         if (it + 1 < nit) {
           if (!(ok = mbar_wait(bar(kQFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
           mma_scores<D>(tmem + kTmS, sK, sQ(s1), kIdSS(BF16));
           mma_commit(bar(kSReady));
         }
-        mma_kmajor_a(tmem + kTmDV, sPt, sDO(s), kIdTS(BF16, D), it > 0);
-        mma_commit(bar(kPtFree));
         if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_packed<NWG>(tmem + kTmDK, tmem + kTmDP, sQ(s), kIdTS(BF16, D), it > 0);
         mma_commit(bar(kQEmpty + s));   // Q(it): last read by dK(it)
-        mma_commit(bar(kDOEmpty + s));  // dO(it): last read by dV(it)
         if (it + 1 < nit) {
           if (!(ok = mbar_wait(bar(kDOFull + s1), ((it + 1) >> 1) & 1, args.err, kErrTimeoutTma))) break;
           tc_fence_after();
@@ -316,24 +304,17 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     const int cbeg = kCols * e;
     const int key = key0 + r;
     const float c = args.scale_log2;
-    // L log2 e and D of block it for this warpgroup's columns (rows padded per head
-    // to a multiple of 128, so whole 16-byte groups are always in bounds).
-    auto lrow = [&](int it) {
-      return args.lse_log2 + (size_t)q_head(it) * args.Npad + q_block(it) * 128 + cbeg;
-    };
-    auto drow = [&](int it) { return args.delta + (size_t)q_head(it) * args.Npad + q_block(it) * 128 + cbeg; };
     bool ok = true;
-    if (r < 2 * kCh) prefetch_l1((r & 1 ? drow(0) : lrow(0)) + (r >> 1) * 32);
     for (int it = 0; it < nit; ++it) {
       const int q0 = q_block(it) * 128;
       const bool diag = args.causal && (key0 + 127 > q0 + koff);  // some key hidden from some query
-      if (it + 1 < nit && r < 2 * kCh) prefetch_l1((r & 1 ? drow(it + 1) : lrow(it + 1)) + (r >> 1) * 32);
-      // ---- P^T = 2^(S^T c - L log2 e), packed into the S^T columns.  The first
-      // chunk's L values are requested before the wait, so their latency hides in it.
-      const float4* L4 = reinterpret_cast<const float4*>(lrow(it));
+      // ---- P^T = 2^(S^T c - L log2 e), packed into the S^T columns.  L log2 e and
+      // D of the block's queries arrive with its Q tile.
+      const uint32_t sl = sLD(it & 1) + 4u * cbeg, sd = sl + 512;
+      if (!(ok = warp_wait(bar(kQFull + (it & 1)), (it >> 1) & 1, args.err, kErrTimeoutTma))) break;
       float4 l4[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + i);
+      for (int i = 0; i < 8; ++i) ld_shared_f4(sl + 16 * i, l4[i]);
       if (!(ok = warp_wait(bar(kSReady), it & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
       float p[kCols];
@@ -343,7 +324,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cbeg + 32 * ch, sv);
         if (ch > 0) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) l4[i] = __ldg(L4 + 8 * ch + i);
+          for (int i = 0; i < 8; ++i) ld_shared_f4(sl + 128 * ch + 16 * i, l4[i]);
         }
         tmem_wait_ld();
         reg_fence32(sv);
@@ -364,33 +345,26 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
             if (key > q0 + cbeg + 32 * ch + x + koff) p[32 * ch + x] = 0.f;
         }
       }
-      tc_fence_before();  // S^T has been read out of TMEM
-      // P^T to shared memory (K-major, key row r), once dV of the previous block has read it.
-      if (it > 0 && !(ok = warp_wait(bar(kPtFree), (it - 1) & 1, args.err, kErrTimeoutMma))) break;
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
-        const uint32_t panel = sPt + (uint32_t)(cbeg / 64) * kPanel;
-        const int c0 = (cbeg % 64 + 32 * ch) / 8;
+        uint32_t pw[16];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float* pp = p + 32 * ch + 8 * k4;
-          st_shared_v4(panel + sw128_offset(r, c0 + k4), pack2<BF16>(pp[0], pp[1]), pack2<BF16>(pp[2], pp[3]),
-                       pack2<BF16>(pp[4], pp[5]), pack2<BF16>(pp[6], pp[7]));
-        }
+        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[32 * ch + 2 * x], p[32 * ch + 2 * x + 1]);
+        tmem_st_32x32b_x16(tmem + lane_base + kTmS + cbeg + 16 * ch, pw);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       warp_arrive(bar(kPFull));
       // ---- dS^T = P^T o (dP^T - D), packed into the dP^T columns
       if (!(ok = warp_wait(bar(kDpReady), it & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
-      const float4* D4 = reinterpret_cast<const float4*>(drow(it));
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         uint32_t dv[32];
         tmem_ld_32x32b_x32(tmem + lane_base + kTmDP + cbeg + 32 * ch, dv);
         float4 d4[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d4[i] = __ldg(D4 + 8 * ch + i);
+        for (int i = 0; i < 8; ++i) ld_shared_f4(sd + 128 * ch + 16 * i, d4[i]);
         tmem_wait_ld();
         reg_fence32(dv);
         uint32_t dw[16];
