@@ -43,6 +43,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  return sms > 0 ? sms : 1;
+}
+
 // Address of the error word on the current device (looked up once per device).
 uint32_t* error_word_ptr() {
   static uint32_t* ptrs[kMaxDevices] = {};
@@ -161,6 +168,25 @@ size_t bwd_workspace_bytes(long long BH, int N, int d) {
 
 using namespace fa;
 
+namespace fa {
+
+int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal) {
+  if (nheads <= 1 || nblocks <= 0) return 1;
+  const long long sms = sm_count();
+  const long long nb = nblocks;
+  const long long work = causal ? nb * (nb + 1) / 2 : nb * nb;  // steps per head; the longest CTA takes nb
+  const long long g_tail = (sms * nb + work - 1) / work;
+  const long long g_l2 = std::max<long long>(1, (48ll << 20) / (long long)std::max<size_t>(bytes_per_head, 1));
+  const long long g = std::min(std::max(g_tail, g_l2), nheads);
+  // Equal groups: a short last group would hold heavy CTAs with too little work
+  // around them.  Take the smallest divisor of nheads in [g, 2g] if there is one.
+  for (long long c = g; c <= std::min(2 * g, nheads); ++c)
+    if (nheads % c == 0) return (int)c;
+  return (int)g;
+}
+
+}  // namespace fa
+
 extern "C" {
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
@@ -189,6 +215,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.head_group = cta_head_group(BH, a.num_qblocks, (size_t)4 * (N_q + N_k) * d, causal != 0);
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
   cudaError_t e = launch_fwd(d, bf16, mq, mk, mv, mo, a, reinterpret_cast<cudaStream_t>(stream));
@@ -257,6 +284,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.head_group_kv = cta_head_group(BHkv, (N_k + 127) / 128, (size_t)4 * ((size_t)a.group * N_q + N_k) * d, causal != 0);
+  a.head_group_q = cta_head_group(BH, (N_q + 127) / 128, (size_t)4 * (N_q + N_k) * d, causal != 0);
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
   cudaError_t e = launch_bwd(d, bf16, mq, mk, mv, mdo, a, reinterpret_cast<cudaStream_t>(stream));

@@ -171,11 +171,12 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   const int N = args.N;
   const int Nk = args.Nk;
 
-  // Work tile: lowest key blocks first across all key/value heads (under the causal
-  // mask they see the most query blocks).  The CTA visits the query blocks of every
+  // Work tile: lowest key blocks first (under the causal mask they see the most
+  // query blocks), key/value heads in groups of args.head_group_kv so the Q and dO
+  // tiles of the running CTAs stay in L2.  The CTA visits the query blocks of every
   // query head of its key/value head's group, so dK, dV of the group sum in TMEM.
-  const int kb = (int)(blockIdx.x / args.BHkv);
-  const int bh_kv = (int)(blockIdx.x % args.BHkv);
+  int kb, bh_kv;
+  grouped_tile(blockIdx.x, args.BHkv, (Nk + 127) / 128, args.head_group_kv, kb, bh_kv);
   const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
   const int key0 = kb * 128;
   const int nqb = (N + 127) / 128;
@@ -476,10 +477,12 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   const int Nk = args.Nk;
 
   // Work tile: the last query blocks first (under the causal mask they see the most
-  // keys), so the final wave holds the lightest work.
+  // keys), so the final wave holds the lightest work; heads in groups of
+  // args.head_group_q.
   const int nqb = (N + 127) / 128;
-  const int qb = nqb - 1 - (int)(blockIdx.x / args.BH);
-  const int bh = (int)(blockIdx.x % args.BH);
+  int qb, bh;
+  grouped_tile(blockIdx.x, args.BH, nqb, args.head_group_q, qb, bh);
+  qb = nqb - 1 - qb;
   const int bh_kv = (bh / args.H) * (args.H / args.group) + (bh % args.H) / args.group;
   const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
   const int q0 = qb * 128;

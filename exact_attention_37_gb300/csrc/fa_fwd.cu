@@ -91,10 +91,12 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
   const int lane = threadIdx.x & 31;
   const int N = args.N;
 
-  // Heaviest query blocks first across all heads (under the causal mask the last
-  // blocks see the most keys), so the last wave holds the lightest work.
-  const int qb = args.num_qblocks - 1 - (int)(blockIdx.x / args.BH);
-  const int bh = (int)(blockIdx.x % args.BH);
+  // Heaviest query blocks first (under the causal mask the last blocks see the most
+  // keys), so the last wave holds the lightest work; heads in groups of
+  // args.head_group, so the K/V tiles of the running CTAs stay in L2.
+  int qb, bh;
+  grouped_tile(blockIdx.x, args.BH, args.num_qblocks, args.head_group, qb, bh);
+  qb = args.num_qblocks - 1 - qb;
   // Key/value head of this query head (grouped-query attention).
   const int bh_kv = (bh / args.H) * (args.H / args.group) + (bh % args.H) / args.group;
   const int row0 = qb * (kBM * NQ);

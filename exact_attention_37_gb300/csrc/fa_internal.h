@@ -19,6 +19,7 @@ struct FwdArgs {
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e): scores go to base 2 with one multiply
   int causal;            // key j hidden from query i when j > i + (Nk - N)
+  int head_group;        // heads per group of the CTA order (cta_head_group)
   uint32_t* err;         // device error word
 };
 
@@ -44,8 +45,20 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   int causal;
+  int head_group_kv;     // key/value heads per group of the dK/dV kernel's CTA order
+  int head_group_q;      // query heads per group of the dQ kernel's CTA order
   uint32_t* err;
 };
+
+// Heads per group of a kernel's CTA order (grouped_tile): the blocks of G heads are
+// launched before those of the next G, so the tiles that concurrently running CTAs
+// read stay in L2.  G is the smallest count whose group gives every SM at least as
+// much work as the group's longest CTA (no tail inside a group), raised until the
+// group's tensors (bytes_per_head each) fill about 48 MB, at most nheads, and
+// then rounded up to a divisor of nheads (within a factor of two) so that every
+// group is equally long.
+// nblocks is the number of CTA blocks per head, each doing up to nblocks steps.
+int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal);
 
 // Rows of Q handled by one forward CTA for head dimension d.
 int fwd_rows_per_cta(int d);

@@ -37,6 +37,22 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- CTA order
+// Linear CTA index -> (block, head) with heads taken in groups of G: every block of
+// heads [g G, g G + G) comes before those of the next group, and inside a group the
+// block index changes slowest (callers map a low block index to their heaviest
+// block).  A bijection for any G >= 1.
+__device__ __forceinline__ void grouped_tile(unsigned idx, int nheads, int nblocks, int G, int& blk, int& head) {
+  G = max(1, min(G, nheads));
+  const unsigned per = (unsigned)G * (unsigned)nblocks;
+  const int g = (int)(idx / per);
+  const unsigned rem = idx - (unsigned)g * per;
+  const int g0 = g * G;
+  const int gg = min(G, nheads - g0);
+  blk = (int)(rem / (unsigned)gg);
+  head = g0 + (int)(rem % (unsigned)gg);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
