@@ -1,7 +1,10 @@
 // Host-buffer entry points: the attention step with its inputs and outputs in
 // host memory, pipelined over chunks of heads on three library-owned streams so
 // that the host-to-device copies of chunk c + 1, the kernels of chunk c and the
-// device-to-host copies of chunk c - 1 overlap.  Heads are independent in both
+// device-to-host copies of chunk c - 1 overlap.  Within a chunk the forward pass
+// starts once Q, K and V are on the device (dO follows), and O and L go back as
+// soon as the forward pass has written them, so the pipeline's fill and drain
+// carry only part of a chunk's copies.  Heads are independent in both
 // passes, so a chunk of heads is a complete problem of its own; each chunk runs
 // through fa_fwd_ex / fa_bwd_ex on a slice of one device scratch region that
 // the caller provides (the library allocates no device memory).
@@ -57,7 +60,8 @@ ScratchLayout layout(long long BH, int N, int d, bool bwd, int max_chunk_heads) 
 struct Pipeline {
   cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
-  cudaEvent_t up_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {};
+  cudaEvent_t qkv_up[kMaxChunks] = {}, dout_up[kMaxChunks] = {};
+  cudaEvent_t fwd_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {};
   bool ready = false;
 };
 
@@ -76,7 +80,9 @@ bool pipeline_for_device(Pipeline** out) {
         cudaEventCreateWithFlags(&p.end, ef) != cudaSuccess)
       return false;
     for (int c = 0; c < kMaxChunks; ++c)
-      if (cudaEventCreateWithFlags(&p.up_done[c], ef) != cudaSuccess ||
+      if (cudaEventCreateWithFlags(&p.qkv_up[c], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.dout_up[c], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.fwd_done[c], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.comp_done[c], ef) != cudaSuccess)
         return false;
     p.ready = true;
@@ -149,27 +155,32 @@ fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const voi
     const int hc = (int)std::min<long long>(per, BH - h0);
     const size_t ot = (size_t)h0 * head_t, bt = (size_t)hc * head_t;
     const size_t ol = (size_t)h0 * head_l, bl = (size_t)hc * head_l;
-    // ---- upload
-    if (!H2D(L.q, q, ot, bt) || !H2D(L.k, k, ot, bt) || !H2D(L.v, v, ot, bt) || (bwd && !H2D(L.dout, dout, ot, bt)))
+    // ---- upload: Q, K, V, then dO (needed only by the backward pass)
+    if (!H2D(L.q, q, ot, bt) || !H2D(L.k, k, ot, bt) || !H2D(L.v, v, ot, bt)) return FA_ERR_CUDA;
+    if (cudaEventRecord(P->qkv_up[c], P->up) != cudaSuccess) return FA_ERR_CUDA;
+    if (bwd && (!H2D(L.dout, dout, ot, bt) || cudaEventRecord(P->dout_up[c], P->up) != cudaSuccess))
       return FA_ERR_CUDA;
-    if (cudaEventRecord(P->up_done[c], P->up) != cudaSuccess) return FA_ERR_CUDA;
     // ---- compute (one chunk of heads is a problem with B = 1, H = hc)
-    if (cudaStreamWaitEvent(P->comp, P->up_done[c], 0) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamWaitEvent(P->comp, P->qkv_up[c], 0) != cudaSuccess) return FA_ERR_CUDA;
     fa_stream_t cs = reinterpret_cast<fa_stream_t>(P->comp);
     fa_status st = fa_fwd_ex(s + L.q + ot, s + L.k + ot, s + L.v + ot, s + L.o + ot,
                              reinterpret_cast<float*>(s + L.lse + ol), 1, hc, hc, N, N, d, scale, causal, dtype, cs);
     if (st != FA_OK) return st;
+    if (cudaEventRecord(P->fwd_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
     if (bwd) {
+      if (cudaStreamWaitEvent(P->comp, P->dout_up[c], 0) != cudaSuccess) return FA_ERR_CUDA;
       st = fa_bwd_ex(s + L.q + ot, s + L.k + ot, s + L.v + ot, s + L.o + ot, s + L.dout + ot,
                      reinterpret_cast<const float*>(s + L.lse + ol), s + L.dq + ot, s + L.dk + ot, s + L.dv + ot,
                      s + L.ws, L.ws_bytes, 1, hc, hc, N, N, d, scale, causal, dtype, cs);
       if (st != FA_OK) return st;
+      if (cudaEventRecord(P->comp_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
     }
-    if (cudaEventRecord(P->comp_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
-    // ---- download
-    if (cudaStreamWaitEvent(P->down, P->comp_done[c], 0) != cudaSuccess) return FA_ERR_CUDA;
+    // ---- download: O and L once the forward pass has written them, then the gradients
+    if (cudaStreamWaitEvent(P->down, P->fwd_done[c], 0) != cudaSuccess) return FA_ERR_CUDA;
     if (!D2H(o, L.o, ot, bt) || !D2H(lse, L.lse, ol, bl)) return FA_ERR_CUDA;
-    if (bwd && (!D2H(dq, L.dq, ot, bt) || !D2H(dk, L.dk, ot, bt) || !D2H(dv, L.dv, ot, bt))) return FA_ERR_CUDA;
+    if (bwd && (cudaStreamWaitEvent(P->down, P->comp_done[c], 0) != cudaSuccess || !D2H(dq, L.dq, ot, bt) ||
+                !D2H(dk, L.dk, ot, bt) || !D2H(dv, L.dv, ot, bt)))
+      return FA_ERR_CUDA;
   }
   return FA_OK;
 }
