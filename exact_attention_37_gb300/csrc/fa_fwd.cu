@@ -277,23 +277,29 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       const float alpha = ex2_approx(fmaf(m, c, -mc));  // 0 when m = -inf
       // p = 2^(s c - m c): packed FMA for the exponent, ex2, packed adds for the row
       // sum.  P goes into the first 64 columns of S_t (two 16-bit values per column),
-      // half a row at a time so the packed words do not all stay live.
+      // part of a row at a time so the packed words do not all stay live.
+      // d = 64 stores a quarter row at a time (fewer live registers; faster there),
+      // d = 128 half a row.
+      constexpr int kPE = D == 64 ? 32 : 64;  // elements of P per store
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pw[32];
+      for (int h = 0; h < 128 / kPE; ++h) {
+        uint32_t pw[kPE / 2];
 #pragma unroll
-        for (int i = 64 * h; i < 64 * h + 64; i += 4) {
+        for (int i = kPE * h; i < kPE * h + kPE; i += 4) {
           float x0, x1, x2, x3;
           fma2(s[i], s[i + 1], c, -mc, x0, x1);
           fma2(s[i + 2], s[i + 3], c, -mc, x2, x3);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           add2(l0, l1, p0, p1);
           add2(l2, l3, p2, p3);
-          pw[(i & 63) >> 1] = pack2<BF16>(p0, p1);
-          pw[((i & 63) >> 1) + 1] = pack2<BF16>(p2, p3);
+          pw[(i % kPE) >> 1] = pack2<BF16>(p0, p1);
+          pw[((i % kPE) >> 1) + 1] = pack2<BF16>(p2, p3);
         }
-        tmem_st_32x32b_x32(tS + 32 * h, pw);
+        if constexpr (kPE == 64)
+          tmem_st_32x32b_x32(tS + 32 * h, pw);
+        else
+          tmem_st_32x32b_x16(tS + 16 * h, pw);
       }
       l = l * alpha + ((l0 + l1) + (l2 + l3));
       tmem_wait_st();
