@@ -91,8 +91,36 @@ bool pipeline_for_device(Pipeline** out) {
   return true;
 }
 
+// Heads per chunk.  An explicit count gives equal chunks (the last may be
+// smaller); the default (chunks <= 0) gives middle chunks of about B*H / 4 heads
+// with first and last chunks of half that, so the pipeline's fill (the first
+// upload) and drain (the last download) are short.  Every chunk but the last is a
+// multiple of `align` heads.  Returns the number of chunks.
+int chunk_plan(long long BH, int chunks, int align, int (&plan)[kMaxChunks]) {
+  auto up = [&](long long x) { return std::max<long long>(align, (x + align - 1) / align * align); };
+  long long mid, first;
+  if (chunks > 0) {
+    chunks = (int)std::min<long long>(std::min(chunks, kMaxChunks), BH);
+    mid = first = up((BH + chunks - 1) / chunks);
+  } else {
+    mid = up((BH + 3) / 4);
+    first = up(mid / 2);
+  }
+  int n = 0;
+  long long h = 0;
+  while (h < BH && n < kMaxChunks - 1) {
+    long long c = n == 0 ? first : mid;
+    if (chunks <= 0 && BH - h - c < first && BH - h - c > 0) c = BH - h - first;  // leave a short last chunk
+    c = std::min(std::max(c, (long long)align), BH - h);
+    plan[n++] = (int)c;
+    h += c;
+  }
+  if (h < BH) plan[n++] = (int)(BH - h);
+  return n;
+}
+
 fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const void* q, const void* k, const void* v,
-                         const void* dout, void* o, float* lse, void* dq, void* dk, void* dv, long long BH, int per,
+                         const void* dout, void* o, float* lse, void* dq, void* dk, void* dv, const int* plan,
                          int chunks, int N, int d, float scale, int causal, fa_dtype dtype, bool bwd);
 
 fa_status run_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse, void* dq,
@@ -102,13 +130,13 @@ fa_status run_host(const void* q, const void* k, const void* v, const void* dout
   const long long BH = (long long)B * H;
   if (BH * N == 0) return FA_OK;
   if (!q || !k || !v || !o || !lse || (bwd && (!dout || !dq || !dk || !dv))) return FA_ERR_INVALID_ARG;
-  if (chunks <= 0) chunks = (int)std::min<long long>(BH, 4);
-  chunks = (int)std::min<long long>(std::min(chunks, kMaxChunks), BH);
-  int per = (int)((BH + chunks - 1) / chunks);  // heads per chunk (the last may be smaller)
-  // Each chunk's L starts on a 16-byte boundary: per * N must be a multiple of 4.
+  // Each chunk's L starts on a 16-byte boundary: chunk starts are multiples of m
+  // heads with m * N a multiple of 4.
   const int m = N % 4 == 0 ? 1 : (N % 2 == 0 ? 2 : 4);
-  per = (int)std::min<long long>((per + m - 1) / m * m, BH);
-  chunks = (int)((BH + per - 1) / per);
+  int plan[kMaxChunks];
+  chunks = chunk_plan(BH, chunks, m, plan);
+  int per = 0;  // heads of the largest chunk
+  for (int c = 0; c < chunks; ++c) per = std::max(per, plan[c]);
   const size_t need = fa_host_scratch_size(B, H, N, d, bwd ? 1 : 0);
   if (need == 0) return FA_ERR_INVALID_ARG;  // invalid sizes (d, limits)
   if (!scratch || scratch_bytes < need) return FA_ERR_WORKSPACE;
@@ -125,7 +153,7 @@ fa_status run_host(const void* q, const void* k, const void* v, const void* dout
       cudaStreamWaitEvent(P->comp, P->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(P->down, P->start, 0) != cudaSuccess)
     return FA_ERR_CUDA;
-  fa_status st = enqueue_chunks(P, L, s, q, k, v, dout, o, lse, dq, dk, dv, BH, per, chunks, N, d, scale, causal,
+  fa_status st = enqueue_chunks(P, L, s, q, k, v, dout, o, lse, dq, dk, dv, plan, chunks, N, d, scale, causal,
                                 dtype, bwd);
   // The caller's stream continues after everything enqueued (also after a failure
   // part-way, so no copy is still in flight when the caller's stream moves on).
@@ -138,7 +166,7 @@ fa_status run_host(const void* q, const void* k, const void* v, const void* dout
 }
 
 fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const void* q, const void* k, const void* v,
-                         const void* dout, void* o, float* lse, void* dq, void* dk, void* dv, long long BH, int per,
+                         const void* dout, void* o, float* lse, void* dq, void* dk, void* dv, const int* plan,
                          int chunks, int N, int d, float scale, int causal, fa_dtype dtype, bool bwd) {
   const size_t head_t = (size_t)N * d * 2;  // bytes of one head of a 16-bit tensor
   const size_t head_l = (size_t)N * 4;      // bytes of one head of L
@@ -150,9 +178,9 @@ fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const voi
     return cudaMemcpyAsync(static_cast<char*>(host) + off, s + dev_off + off, bytes, cudaMemcpyDeviceToHost,
                            P->down) == cudaSuccess;
   };
-  for (int c = 0; c < chunks; ++c) {
-    const long long h0 = (long long)c * per;
-    const int hc = (int)std::min<long long>(per, BH - h0);
+  long long h0 = 0;
+  for (int c = 0; c < chunks; h0 += plan[c++]) {
+    const int hc = plan[c];
     const size_t ot = (size_t)h0 * head_t, bt = (size_t)hc * head_t;
     const size_t ol = (size_t)h0 * head_l, bl = (size_t)hc * head_l;
     // ---- upload: Q, K, V, then dO (needed only by the backward pass)

@@ -184,8 +184,10 @@ fa_status fa_check_device_status(fa_stream_t stream);
  * Host-buffer entry points (a runtime convenience; the attention method has no
  * counterpart): the forward pass, or the forward and backward pass, of a
  * problem whose inputs and outputs live in host memory.  The B*H heads are split
- * into `chunks` chunks of consecutive heads (chunks <= 0: min(B*H, 4); at most
- * 64); chunk c's host-to-device copies, kernels and device-to-host copies run on
+ * into `chunks` chunks of consecutive heads (equal chunks, at most 64; with
+ * chunks <= 0, middle chunks of about B*H / 4 heads between a first and a last
+ * chunk of half that size, which shortens the pipeline's fill and drain);
+ * chunk c's host-to-device copies, kernels and device-to-host copies run on
  * three library-owned streams, so copies of one chunk overlap the kernels of
  * another.  Every chunk is an independent problem (B = 1, H = heads of the
  * chunk) computed by fa_fwd_ex / fa_bwd_ex, so the results equal those of the
