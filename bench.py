@@ -1,6 +1,7 @@
 #!/usr/bin/env python3
-"""Attention throughput on GB300: one step = forward + backward (D pre-pass, main
-backward kernel, dQ conversion) of exact causal attention over one batch.
+"""Attention throughput on GB300: one step = forward + backward (D pre-pass, then
+the dK/dV and dQ kernels for d = 64, 128, or the main kernel and the dQ
+conversion for d = 256) of exact causal attention over one batch.
 
 Workload (default): B=2, H=16, N=8192, d=128, bf16, causal, Q/K/V = 0.5*N(0,1),
 dO = N(0,1) (seeded, synthetic).  Prints one JSON line.
@@ -12,8 +13,10 @@ causal mask.  ``value`` is forward+backward TFLOP/s with inputs resident in
 device memory; ``e2e`` is the same metric through the C-ABI with host buffers
 (pinned host->device copies of Q, K, V, dO and device->host copies of O, L, dQ,
 dK, dV inside the timed region).  L2 is flushed (a 256 MB write) before every
-timed step.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample
-of the same workload.
+timed step.  The secondary bound, the exponentials (one per visible pair in each
+pass), is reported as exp/s and as a fraction of the MUFU rate at the sampled SM
+clock.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload.
 """
 from __future__ import annotations
 
@@ -171,6 +174,11 @@ def reduce_max(x, world, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# ex2.approx.f32 throughput measured on this part (one probe CTA per SM): the
+# secondary bound of the method, one exponential per visible (query, key) pair.
+MUFU_EX2_PER_CLK_PER_SM = 32
 
 
 def visible_pairs(w, rows):
@@ -415,6 +423,20 @@ def main():
                 "frac": achieved / peak, "traffic": profile_traffic(tag),
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
 
+    # Exponentials: one per visible pair in the forward pass and the same again in
+    # the backward pass (algorithmic counts; the two-kernel backward for d = 64, 128
+    # evaluates them twice, once in each kernel).  Peak: the MUFU rate at the SM
+    # clock sampled under load.
+    clk = clocks.summary()
+    sm_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mufu_peak = MUFU_EX2_PER_CLK_PER_SM * n_sms * sm_mhz * 1e6 if sm_mhz else None
+    exps = B * H * visible_pairs(w, range(w.N))
+
+    def exp_rate(ms):
+        r = exps / (ms / 1e3)
+        return {"exp_per_s": r, "exp_frac_of_mufu": (r / mufu_peak) if mufu_peak else None}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cv, cdt, heads = cpu_oracle_sample(w, q, k, v, do, backward=not fwd_only)
@@ -428,14 +450,17 @@ def main():
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-                       "step": "fwd" if fwd_only else ("fwd + bwd (pre, dK/dV kernel, dQ kernel)" if d == 128
+                       "step": "fwd" if fwd_only else ("fwd + bwd (pre, dK/dV kernel, dQ kernel)" if d in (64, 128)
                                                         else "fwd + bwd (pre, main, dq convert)"),
                        "l2": "256 MB flush write before every step", "parallelism": f"replicas x{world}"},
-            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"])},
+            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"]),
+                    **exp_rate(fwd_avg)},
             "bwd": None if fwd_only else {
                 "tflops": flops_bwd / (statistics.mean(bwd_ms) / 1e3) / 1e12, "ms": statistics.mean(bwd_ms),
                 "main_kernel_ms": bwd_main_avg,
-                "main_kernel_frac_of_peak_sustained": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / peak},
+                "main_kernel_frac_of_peak_sustained": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / peak,
+                **exp_rate(bwd_main_avg)},
+            "mufu_peak_exp_per_s": mufu_peak,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -443,7 +468,7 @@ def main():
                     "path": f"{'fa_fwd_host' if fwd_only else 'fa_fwd_bwd_host'} (C ABI, pinned host buffers, "
                             f"{args.chunks if args.chunks > 0 else 'default'} head chunks)"},
             "gpu_launches": (1 if fwd_only else 4) * K,
-            "clocks": clocks.summary(),
+            "clocks": clk,
         }
         print(json.dumps(out))
     if world > 1:
