@@ -132,14 +132,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int N = args.N;
 
-  // Work tile: the lowest key blocks first across all heads (under the causal mask
-  // they have the most query blocks), so the last wave holds the lightest work.
-  // One CTA per (key/value head, key block, column half); it visits the query
-  // blocks of every query head of its group, so dK and dV of a shared key/value
-  // head are summed in TMEM without any cross-CTA reduction.
-  const int tiles_per_kb = args.BHkv * kHalves;
-  const int kb = (int)(blockIdx.x / tiles_per_kb);
-  const int rem = (int)(blockIdx.x % tiles_per_kb);
+  // Work tile: the lowest key blocks first (under the causal mask they have the
+  // most query blocks), so the last wave holds the lightest work; key/value heads
+  // in groups of args.head_group_kv (both column halves of a head in one group), so
+  // the tiles of the running CTAs stay in L2.  One CTA per (key/value head, key
+  // block, column half); it visits the query blocks of every query head of its
+  // group, so dK and dV of a shared key/value head are summed in TMEM without any
+  // cross-CTA reduction.
+  int kb, rem;
+  grouped_tile(blockIdx.x, args.BHkv * kHalves, (args.Nk + kBN - 1) / kBN, args.head_group_kv * kHalves, kb, rem);
   const int bh_kv = rem / kHalves;
   const int half = rem % kHalves;
   const int Nk = args.Nk;
