@@ -25,6 +25,8 @@ def built():
     [
         Workload("host_d128", 2, 3, 777, 128, "bf16", True, 1.0, (701, 702, 703, 704)),
         Workload("host_d64_odd_n", 1, 5, 513, 64, "fp16", False, 1.0, (705, 706, 707, 708)),
+        # 16 heads, N a multiple of 4: the default plan is 2, 4, 4, 4, 2 heads
+        Workload("host_d128_16_heads", 2, 8, 256, 128, "bf16", True, 1.0, (709, 710, 711, 712)),
     ],
     ids=lambda w: w.name,
 )
