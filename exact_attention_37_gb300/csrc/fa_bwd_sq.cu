@@ -124,7 +124,7 @@ struct Smem {
 };
 enum : int {
   kKVFull = 0,
-  kQFull = 1,    // two
+  kQFull = 1,    // two: a Q tile with the L log2 e and D rows of its query block
   kQEmpty = 3,   // two
   kDOFull = 5,   // two
   kDOEmpty = 7,  // two
