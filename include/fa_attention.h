@@ -152,8 +152,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * counterpart to this entry point; it only changes where the scratch lives.)
  *
  * Arguments, layout, results and errors are those of fa_bwd, minus the
- * workspace pair.  The scratch (the fp32 dQ accumulator and the fp32 row
- * vectors, fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
+ * workspace pair.  The scratch (the fp32 row vectors and, for d = 256, the fp32
+ * dQ accumulator: fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
  * library's device memory, allocated when the library's device code is loaded
  * and held by every GPU that loads it until the process exits.  Calls whose
  * scratch would exceed 32 MiB (33554432 bytes) return FA_ERR_WORKSPACE and
@@ -164,7 +164,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * that device current); make that first call before any stream capture.  No
  * call allocates: no cudaMalloc, cudaFree or allocating library routine.  Every
  * call overwrites the whole scratch region it uses before reading it (the D
- * pre-pass zeroes the dQ accumulator), so stale contents from an earlier call
+ * pre-pass writes every row vector and, for d = 256, zeroes the dQ
+ * accumulator), so stale contents from an earlier call
  * never leak into a result.  All calls share the one array: two calls whose
  * kernels overlap on the GPU (different streams, no ordering between them)
  * race on it and give wrong gradients; order them on one stream or with events.
