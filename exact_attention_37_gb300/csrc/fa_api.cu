@@ -303,7 +303,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
 namespace fa {
 namespace {
-// Fixed scratch of fa_bwd_noalloc (fp32 dQ accumulator + fp32 D rows).  Its
+// Fixed scratch of fa_bwd_noalloc (the backward workspace: fp32 L log2 e and D
+// rows, plus the fp32 dQ accumulator for d = 256).  Its
 // name in host code is only a host-side stand-in; the device address comes
 // from cudaGetSymbolAddress on each device.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
