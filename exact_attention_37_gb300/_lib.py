@@ -36,6 +36,8 @@ SIGNATURES = {
                        _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_host_scratch_size": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_host_chunk_plan": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "fa_cta_head_group": (_i, [ctypes.c_longlong, _i, _sz, _i, _i]),
     "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_fwd_bwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _i,
                              _vp]),
@@ -167,6 +169,23 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool
 
 def fa_host_scratch_size(B: int, H: int, N: int, d: int, backward: bool = True) -> int:
     return int(load().fa_host_scratch_size(B, H, N, d, int(bool(backward))))
+
+
+def fa_host_chunk_plan(B: int, H: int, N: int, chunks: int = 0) -> list:
+    """Heads per chunk of the host-buffer pipeline for these sizes (host query)."""
+    plan = (ctypes.c_int * 64)()
+    n = load().fa_host_chunk_plan(B, H, N, chunks, plan, 64)
+    if n < 0:
+        raise FaError("fa_host_chunk_plan", 1)
+    return list(plan[:n])
+
+
+def fa_cta_head_group(nheads: int, nblocks: int, bytes_per_head: int, causal: bool, num_sms: int) -> int:
+    """Heads per group of the kernels' CTA order (host query)."""
+    g = load().fa_cta_head_group(nheads, nblocks, bytes_per_head, int(bool(causal)), num_sms)
+    if g < 0:
+        raise FaError("fa_cta_head_group", 1)
+    return int(g)
 
 
 def _host_tensors(*ts):

@@ -170,9 +170,9 @@ using namespace fa;
 
 namespace fa {
 
-int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal) {
+int cta_head_group_for(long long nheads, int nblocks, size_t bytes_per_head, bool causal, int num_sms) {
   if (nheads <= 1 || nblocks <= 0) return 1;
-  const long long sms = sm_count();
+  const long long sms = std::max(num_sms, 1);
   const long long nb = nblocks;
   const long long work = causal ? nb * (nb + 1) / 2 : nb * nb;  // steps per head; the longest CTA takes nb
   const long long g_tail = (sms * nb + work - 1) / work;
@@ -183,6 +183,10 @@ int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool ca
   for (long long c = g; c <= std::min(2 * g, nheads); ++c)
     if (nheads % c == 0) return (int)c;
   return (int)g;
+}
+
+int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal) {
+  return cta_head_group_for(nheads, nblocks, bytes_per_head, causal, sm_count());
 }
 
 }  // namespace fa
@@ -342,6 +346,11 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   if (!scratch) return FA_ERR_CUDA;
   return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes, B, H, N, d, scale, causal, dtype,
                 stream);
+}
+
+int fa_cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, int causal, int num_sms) {
+  if (nheads < 1 || nblocks < 0) return -1;
+  return cta_head_group_for(nheads, nblocks, bytes_per_head, causal != 0, num_sms > 0 ? num_sms : sm_count());
 }
 
 fa_status fa_check_device_status(fa_stream_t stream) {

@@ -98,6 +98,7 @@ bool pipeline_for_device(Pipeline** out) {
 // multiple of `align` heads.  Returns the number of chunks.
 int chunk_plan(long long BH, int chunks, int align, int (&plan)[kMaxChunks]) {
   auto up = [&](long long x) { return std::max<long long>(align, (x + align - 1) / align * align); };
+  auto down = [&](long long x) { return std::max<long long>(align, x / align * align); };
   long long mid, first;
   if (chunks > 0) {
     chunks = (int)std::min<long long>(std::min(chunks, kMaxChunks), BH);
@@ -110,8 +111,11 @@ int chunk_plan(long long BH, int chunks, int align, int (&plan)[kMaxChunks]) {
   long long h = 0;
   while (h < BH && n < kMaxChunks - 1) {
     long long c = n == 0 ? first : mid;
-    if (chunks <= 0 && BH - h - c < first && BH - h - c > 0) c = BH - h - first;  // leave a short last chunk
-    c = std::min(std::max(c, (long long)align), BH - h);
+    // Default plan: when what would remain after this chunk is shorter than a
+    // first chunk, take less now (still a multiple of `align`), so the last chunk
+    // stays about as short as the first.
+    if (chunks <= 0 && BH - h - c < first && BH - h - c > 0) c = down(BH - h - first);
+    c = std::min(c, BH - h);  // only the last chunk can be cut short here
     plan[n++] = (int)c;
     h += c;
   }
@@ -219,6 +223,18 @@ fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const voi
 using namespace fa;
 
 extern "C" {
+
+int fa_host_chunk_plan(int B, int H, int N, int chunks, int* plan, int capacity) {
+  if (B < 0 || H < 0 || N < 0 || capacity < 0) return -1;
+  const long long BH = (long long)B * H;
+  if (BH * N == 0) return 0;
+  const int m = N % 4 == 0 ? 1 : (N % 2 == 0 ? 2 : 4);
+  int p[kMaxChunks];
+  const int n = chunk_plan(BH, chunks, m, p);
+  if (plan && capacity >= n)
+    for (int c = 0; c < n; ++c) plan[c] = p[c];
+  return n;
+}
 
 size_t fa_host_scratch_size(int B, int H, int N, int d, int with_backward) {
   if (B < 0 || H < 0 || N < 0 || (d != 64 && d != 128 && d != 256)) return 0;

@@ -208,12 +208,36 @@ fa_status fa_check_device_status(fa_stream_t stream);
  * several host threads are serialized by the library.
  */
 size_t fa_host_scratch_size(int B, int H, int N, int d, int with_backward);
+
+/*
+ * The chunk plan fa_fwd_host / fa_fwd_bwd_host use for these sizes and `chunks`
+ * (a host query; it touches no device): writes the heads of each chunk, in
+ * order, to plan[0 .. n-1] when plan is non-null and capacity >= n, and returns
+ * n (at most 64).  Every chunk but the last starts at a head h whose first row
+ * h*N keeps L 16-byte aligned.  Returns 0 for an empty problem and -1 for
+ * negative sizes.
+ */
+int fa_host_chunk_plan(int B, int H, int N, int chunks, int* plan, int capacity);
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dev_scratch,
                       size_t scratch_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
                       int chunks, fa_stream_t stream);
 fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
                           void* dq, void* dk, void* dv, void* dev_scratch, size_t scratch_bytes, int B, int H, int N,
                           int d, float scale, int causal, fa_dtype dtype, int chunks, fa_stream_t stream);
+
+/*
+ * Heads per group of the CTA order the kernels use (a host query; it touches no
+ * device when num_sms > 0).  The main kernels take heads in groups of G, the
+ * heaviest blocks first inside a group, so the tiles that concurrently running
+ * CTAs read stay in L2.  G is the smallest head count whose group gives each of
+ * num_sms SMs at least as much work as the group's longest CTA (nblocks blocks
+ * per head, each doing up to nblocks steps; under the causal mask the steps fall
+ * to 1), raised until the group's tensors (bytes_per_head each) fill about 48 MB,
+ * at most nheads, and then rounded up to a divisor of nheads within a factor of
+ * two when there is one.  num_sms <= 0 uses the current device's SM count.
+ * Returns -1 for nheads < 1 or nblocks < 0.
+ */
+int fa_cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, int causal, int num_sms);
 
 /*
  * Failure-detection self-test (a diagnostic; the attention method has no

@@ -158,3 +158,52 @@ def test_host_entry_points_validate_on_the_host(lib):
     assert lib.fa_fwd_bwd_host(*([p] * 9), vp(0), 1 << 30, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 4
     assert lib.fa_fwd_bwd_host(*([p] * 9), p, 100, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 4
     assert lib.fa_fwd_host(*([p] * 5), vp(4096 + 16), 1 << 30, 1, 2, 64, 64, 0.1, 0, 1, 0, None) == 3
+
+
+@pytest.mark.parametrize("B,H,N,chunks", [(2, 16, 8192, 0), (4, 16, 2048, 0), (1, 1, 256, 0), (2, 3, 777, 0),
+                                          (1, 5, 513, 0), (2, 8, 256, 0), (2, 16, 8192, 4), (2, 16, 8192, 3),
+                                          (2, 16, 8192, 64), (1, 100, 1000, 64), (5, 7, 33, 0), (8, 125, 64, 0)])
+def test_host_chunk_plan_covers_every_head_once(lib, B, H, N, chunks):
+    plan = _lib.fa_host_chunk_plan(B, H, N, chunks)
+    BH = B * H
+    assert sum(plan) == BH and all(c > 0 for c in plan) and 1 <= len(plan) <= 64
+    # every chunk start keeps L (B*H rows of N floats) 16-byte aligned
+    starts = [sum(plan[:i]) for i in range(len(plan))]
+    assert all(s * N % 4 == 0 for s in starts)
+    if chunks > 0:  # an explicit count: equal chunks, the last one possibly smaller
+        assert len(plan) <= max(chunks, 1) or len(plan) <= 64
+        assert all(c == plan[0] for c in plan[:-1]) and plan[-1] <= plan[0]
+
+
+def test_host_chunk_plan_default_is_tapered(lib):
+    assert _lib.fa_host_chunk_plan(2, 16, 8192) == [4, 8, 8, 8, 4]
+    assert _lib.fa_host_chunk_plan(4, 16, 2048) == [8, 16, 16, 16, 8]
+    assert _lib.fa_host_chunk_plan(2, 16, 8192, 4) == [8, 8, 8, 8]
+    assert _lib.fa_host_chunk_plan(1, 1, 256) == [1]
+    assert lib.fa_host_chunk_plan(0, 4, 128, 0, None, 0) == 0
+    assert lib.fa_host_chunk_plan(-1, 4, 128, 0, None, 0) == -1
+
+
+@pytest.mark.parametrize("nheads", [1, 2, 7, 32, 64, 96, 1000])
+@pytest.mark.parametrize("nblocks", [1, 16, 64, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_cta_head_group_properties(lib, nheads, nblocks, causal):
+    sms, bph = 152, 8 << 20
+    g = _lib.fa_cta_head_group(nheads, nblocks, bph, causal, sms)
+    assert 1 <= g <= nheads
+    work = nblocks * (nblocks + 1) // 2 if causal else nblocks * nblocks
+    g_tail = -(-sms * nblocks // work)
+    g_l2 = max(1, (48 << 20) // bph)
+    g0 = min(max(g_tail, g_l2), nheads)
+    assert g >= g0  # no tail inside a group, and about 48 MB of tensors per group
+    divisors = [c for c in range(g0, min(2 * g0, nheads) + 1) if nheads % c == 0]
+    assert g == (divisors[0] if divisors else g0)  # equal groups whenever a divisor is near
+
+
+def test_cta_head_group_at_the_workload_shapes(lib):
+    # long workload (32 heads, 8 MB of Q, K, V, O or dO per head), 152 SMs
+    assert _lib.fa_cta_head_group(32, 32, 8 << 20, True, 152) == 16   # forward: 256-row blocks
+    assert _lib.fa_cta_head_group(32, 64, 8 << 20, True, 152) == 8    # backward: 128-row blocks
+    assert _lib.fa_cta_head_group(32, 256, 32 << 20, True, 152) == 2  # 32k context, backward
+    assert _lib.fa_cta_head_group(64, 16, 1 << 20, False, 152) == 64  # small heads: one group
+    assert lib.fa_cta_head_group(0, 4, 1, 0, 152) == -1

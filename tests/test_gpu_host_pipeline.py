@@ -27,6 +27,9 @@ def built():
         Workload("host_d64_odd_n", 1, 5, 513, 64, "fp16", False, 1.0, (705, 706, 707, 708)),
         # 16 heads, N a multiple of 4: the default plan is 2, 4, 4, 4, 2 heads
         Workload("host_d128_16_heads", 2, 8, 256, 128, "bf16", True, 1.0, (709, 710, 711, 712)),
+        # 35 heads of odd length: chunk starts must be multiples of 4 heads (L stays
+        # 16-byte aligned); the default plan is 8, 12, 4, 11
+        Workload("host_d64_35_heads", 5, 7, 33, 64, "fp16", True, 1.0, (713, 714, 715, 716)),
     ],
     ids=lambda w: w.name,
 )
