@@ -28,6 +28,8 @@ from ._lib import (  # noqa: F401
     fa_fwd,
     fa_fwd_bwd_host,
     fa_fwd_host,
+    fa_cta_head_group,
+    fa_host_chunk_plan,
     fa_host_scratch_size,
     fa_status_string,
     fa_version,
@@ -35,7 +37,8 @@ from ._lib import (  # noqa: F401
 )
 
 __all__ = ["forward", "backward", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_status",
-           "fa_fwd_host", "fa_fwd_bwd_host", "fa_host_scratch_size", "FaError", "load"]
+           "fa_fwd_host", "fa_fwd_bwd_host", "fa_host_scratch_size", "fa_host_chunk_plan", "fa_cta_head_group",
+           "FaError", "load"]
 
 
 def _default_scale(d: int) -> float:
