@@ -170,7 +170,8 @@ using namespace fa;
 
 namespace fa {
 
-int cta_head_group_for(long long nheads, int nblocks, size_t bytes_per_head, bool causal, int num_sms) {
+// cta_head_group for a given number of SMs (also the host query fa_cta_head_group).
+static int cta_head_group_for(long long nheads, int nblocks, size_t bytes_per_head, bool causal, int num_sms) {
   if (nheads <= 1 || nblocks <= 0) return 1;
   const long long sms = std::max(num_sms, 1);
   const long long nb = nblocks;

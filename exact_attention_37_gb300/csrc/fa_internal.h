@@ -59,8 +59,6 @@ struct BwdArgs {
 // group is equally long.
 // nblocks is the number of CTA blocks per head, each doing up to nblocks steps.
 int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal);
-// The same for a given number of SMs (the host query fa_cta_head_group).
-int cta_head_group_for(long long nheads, int nblocks, size_t bytes_per_head, bool causal, int num_sms);
 
 // Rows of Q handled by one forward CTA for head dimension d.
 int fwd_rows_per_cta(int d);
