@@ -181,6 +181,27 @@ def reduce_max(x, world, device):
 MUFU_EX2_PER_CLK_PER_SM = 32
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (the model name, or on Arm the
+    implementer and part codes), for the CPU baseline's record."""
+    import platform
+
+    try:
+        lines = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.processor() or platform.machine()
+    for key in ("model name", "Model"):
+        for line in lines:
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    found = {}
+    for line in lines:
+        for key in ("CPU implementer", "CPU part"):
+            if line.startswith(key) and ":" in line and key not in found:
+                found[key] = line.split(":", 1)[1].strip()
+    return f"{platform.machine()}, implementer {found.get('CPU implementer', '?')}, part {found.get('CPU part', '?')}"
+
+
 def visible_pairs(w, rows):
     """(query, key) pairs the mask leaves visible in the given query rows of one head."""
     import numpy as np
@@ -266,7 +287,8 @@ def run_reference(args, w, backward):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "input_dtype": w.dtype, "step": "fwd + bwd" if backward else "fwd"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -440,7 +462,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cv, cdt, heads = cpu_oracle_sample(w, q, k, v, do, backward=not fwd_only)
-        cpu = {"value": cv, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": cv, "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
                "sample": f"{heads} head(s) of the {w.B * w.H}, forward{'' if fwd_only else ' + backward'}, "
                          f"fp64 numpy, {cdt:.1f} s; FLOPs of the visible pairs"}
 
