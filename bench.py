@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Attention throughput on GB300: one step = forward + backward (D pre-pass, then
-the dK/dV and dQ kernels for d = 64, 128, or the main kernel and the dQ
-conversion for d = 256) of exact causal attention over one batch.
+the dK/dV and dQ kernels for d = 64, 128, or the one launch of dK, dV and dQ CTAs
+for d = 256) of exact causal attention over one batch.
 
 Workload (default): B=2, H=16, N=8192, d=128, bf16, causal, Q/K/V = 0.5*N(0,1),
 dO = N(0,1) (seeded, synthetic).  Prints one JSON line.
@@ -92,55 +92,118 @@ def profile_traffic(kernel_tag):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 50 ms while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons of one GPU, sampled every few
+    milliseconds by a host thread through NVML (the driver's libnvidia-ml, read
+    only), from before the warm-up until after the e2e leg.  Samples taken while
+    ``busy`` is set (a timed region is running) are the ones under load.  Falls
+    back to an ``nvidia-smi --query-gpu`` loop if NVML cannot be opened."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+    def __init__(self, pci_bus_id, uuid=None, period_s=0.004):
+        self.pci = pci_bus_id
+        self.uuid = uuid
+        self.period = period_s
+        self.samples = []  # (busy, sm_mhz, reason bits)
+        self.max_mhz = None
+        self.busy = False
+        self.source = None
+        self._stop = False
+        self._thread = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        found = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h)) == 0
+        if not found and self.uuid:
+            found = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not found:
+            raise OSError("no NVML handle for " + self.pci)
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+            self.max_mhz = float(mx.value)
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, get_reasons
 
     def __enter__(self):
+        import threading
+
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            lib, h, get_reasons = self._nvml()
+            self.source = "nvml"
+
+            def run():
+                import ctypes
+
+                mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop:
+                    busy = self.busy
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                        r = get_reasons(h, ctypes.byref(bits))
+                        self.samples.append((busy, float(mhz.value), int(bits.value) if r == 0 else 0))
+                    time.sleep(self.period)
+
+            self._thread = threading.Thread(target=run, daemon=True)
+            self._thread.start()
         except Exception:
-            self.proc = None
+            self._start_smi()
         return self
 
+    def _start_smi(self):
+        import threading
+
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", self.pci, f"--query-gpu={self.QUERY}",
+                                           "--format=csv,noheader,nounits", "-lms", "20"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self._proc = None
+            return
+        self.source = "nvidia-smi"
+        bits = (0x8, 0x40, 0x20, 0x4)
+
+        def run():
+            for line in self._proc.stdout:
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    mhz, self.max_mhz = float(parts[0]), float(parts[1])
+                except (ValueError, IndexError):
+                    continue
+                r = sum(b for b, v in zip(bits, parts[2:6]) if v.lower() == "active")
+                self.samples.append((self.busy, mhz, r))
+
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop = True
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
-            self.f.close()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"], "samples": 0}
+        load = [s for s in self.samples if s[0]] or self.samples
+        reasons = sorted({n for _, _, r in load for b, n in self.REASONS.items() if r & b})
+        return {"sm_mhz": statistics.median(m for _, m, _ in load), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(m for _, m, _ in load), "reasons": reasons, "samples": len(load),
+                "samples_total": len(self.samples), "source": self.source}
 
 
 def dist_setup():
@@ -353,17 +416,27 @@ def main():
         fa.fa_fwd(qd, kd, vd, od, lse, w.scale, w.causal)
         run_bwd()
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    fa.fa_check_device_status()
+    props = torch.cuda.get_device_properties(dev)
+    pci = getattr(props, "pci_bus_id", None)
+    pci = (f"{getattr(props, 'pci_domain_id', 0):08x}:{pci:02x}:{getattr(props, 'pci_device_id', 0):02x}.0"
+           if isinstance(pci, int) else str(local))
+    uuid = getattr(props, "uuid", None)
+    uuid = None if uuid is None else (str(uuid) if str(uuid).startswith("GPU-") else f"GPU-{uuid}")
+    clocks = ClockSampler(pci, uuid)
+    clocks.__enter__()
+    try:
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        fa.fa_check_device_status()
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    fa.fa_profile_begin(2 * K)
-    with ClockSampler(local) as clocks:
+        K = args.steps
+        n_launch = 1 if fwd_only else (3 if d in (64, 128) else 2)  # main-kernel launches per step
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        fa.fa_profile_begin(n_launch * K)
         barrier(world)
         torch.cuda.synchronize()
+        clocks.busy = True
         for i in range(K):
             flush.zero_()
             e0, e1, e2 = ev[i]
@@ -373,85 +446,115 @@ def main():
             run_bwd()
             e2.record(stream)
         torch.cuda.synchronize()
+        clocks.busy = False
         barrier(world)
-    kernels = fa.fa_profile_end()
-    fa.fa_check_device_status()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    fwd_kernel_ms = [ms for kind, ms in kernels if kind == "fwd"]
-    bwd_main_ms = [ms for kind, ms in kernels if kind == "bwd"]
-    total_ms = reduce_max(sum(step_ms), world, dev)
-    ms_per_step = total_ms / K
+        kernels = fa.fa_profile_end()
+        fa.fa_check_device_status()
+        step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+        fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+        per_kind = {}
+        for kind, ms in kernels:
+            per_kind.setdefault(kind, []).append(ms)
+        total_ms = reduce_max(sum(step_ms), world, dev)
+        ms_per_step = total_ms / K
 
-    flops_fwd = attention_flops(w, backward=False)
-    flops_step = flops_fwd if fwd_only else attention_flops(w)
-    value = world * flops_step * K / (total_ms / 1e3) / 1e12
+        flops_fwd = attention_flops(w, backward=False)
+        flops_step = flops_fwd if fwd_only else attention_flops(w)
+        value = world * flops_step * K / (total_ms / 1e3) / 1e12
 
-    # ---- end to end through the C ABI with host buffers: fa_fwd_host / fa_fwd_bwd_host take
-    # pinned host tensors and pipeline head chunks (copies in, kernels, copies out) on the
-    # library's streams; the caller's stream waits for the whole step
-    pin = lambda t: t.pin_memory()
-    qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
-    oh = torch.empty_like(q).pin_memory()
-    lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    host_in = [qh, kh, vh] + ([] if fwd_only else [doh])
-    host_out = [oh, lseh]
-    if not fwd_only:
-        dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v))
-        host_out += [dqh, dkh, dvh]
-    h2d = sum(x.numel() * x.element_size() for x in host_in)
-    d2h = sum(x.numel() * x.element_size() for x in host_out)
-    scratch = torch.empty(fa.fa_host_scratch_size(B, H, N, d, not fwd_only), dtype=torch.uint8, device=dev)
+        # ---- end to end through the C ABI with host buffers: fa_fwd_host / fa_fwd_bwd_host take
+        # pinned host tensors and pipeline head chunks (copies in, kernels, copies out) on the
+        # library's streams; the caller's stream waits for the whole step
+        pin = lambda t: t.pin_memory()
+        qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
+        oh = torch.empty_like(q).pin_memory()
+        lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        host_in = [qh, kh, vh] + ([] if fwd_only else [doh])
+        host_out = [oh, lseh]
+        if not fwd_only:
+            dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, k, v))
+            host_out += [dqh, dkh, dvh]
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        scratch = torch.empty(fa.fa_host_scratch_size(B, H, N, d, not fwd_only), dtype=torch.uint8, device=dev)
 
-    def host_step():
-        if fwd_only:
-            fa.fa_fwd_host(qh, kh, vh, oh, lseh, scratch, w.scale, w.causal, args.chunks)
-        else:
-            fa.fa_fwd_bwd_host(qh, kh, vh, doh, oh, lseh, dqh, dkh, dvh, scratch, w.scale, w.causal, args.chunks)
+        def host_step():
+            if fwd_only:
+                fa.fa_fwd_host(qh, kh, vh, oh, lseh, scratch, w.scale, w.causal, args.chunks)
+            else:
+                fa.fa_fwd_bwd_host(qh, kh, vh, doh, oh, lseh, dqh, dkh, dvh, scratch, w.scale, w.causal,
+                                   args.chunks)
 
-    for _ in range(2):
-        host_step()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    torch.cuda.synchronize()
-    barrier(world)
-    for i in range(K):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        host_step()
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    fa.fa_check_device_status()
+        for _ in range(2):
+            host_step()
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks.busy = True
+        for i in range(K):
+            flush.zero_()
+            e2e_ev[i][0].record(stream)
+            host_step()
+            e2e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        clocks.busy = False
+        barrier(world)
+        fa.fa_check_device_status()
+    finally:
+        clocks.__exit__(None, None, None)
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
     e2e_value = world * flops_step * K / (e2e_ms / 1e3) / 1e12
 
-    # ---- roofline of the dominant kernel
+    # ---- roofline: every main kernel on its own, the dominant one as the `roofline` entry.
+    # Algorithmic FLOPs (forward 4d per visible pair, backward 10d: the five products S, dP,
+    # dV, dK, dQ at 2d each) are attributed to the kernel that produces the product's
+    # result for an output: the dK/dV kernel owns S, dP, dV, dK (4 of the 5), the dQ
+    # kernel only dQ (its S and dP are recomputation: executed, not algorithmic); the
+    # single d = 256 backward launch owns all five.  `executed_tflops` counts every
+    # product a kernel runs: 3 of 5 for the dQ kernel; for d = 256, 8 of 5 (S in the
+    # dK, dV and dQ CTAs, dP in the dK and dQ CTAs, and the three gradients).
     peaks, peak_src = load_peaks()
-    fwd_avg = statistics.mean(fwd_kernel_ms)
-    bwd_main_avg = statistics.mean(bwd_main_ms) if bwd_main_ms else 0.0
+    timed_s = total_ms / 1e3
+    burst = float(peaks["bf16_tflops"])
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    # a timed region under a second is a burst; seconds-long loops settle at the sustained rate
+    peak, peak_kind = (burst, "burst") if timed_s < 1.0 else (sustained, "sustained")
     flops_bwd = attention_flops(w) - flops_fwd
-    if bwd_main_avg >= fwd_avg:
-        # the main backward launches between the library's marks: dK/dV + dQ kernels
-        # for d = 64 and 128, the fused kernel for d = 256
-        dom, dom_ms, dom_flops = "fa_bwd_main", bwd_main_avg, flops_bwd
-    else:
-        dom, dom_ms, dom_flops = "fa_fwd_kernel", fwd_avg, flops_fwd
+    own = {"fwd": (flops_fwd, flops_fwd), "bwd_kv": (0.8 * flops_bwd, 0.8 * flops_bwd),
+           "bwd_q": (0.2 * flops_bwd, 0.6 * flops_bwd), "bwd_fused": (flops_bwd, 1.6 * flops_bwd)}
+    names = {"fwd": "fa_fwd_kernel", "bwd_kv": "fa_bwd_kv_kernel", "bwd_q": "fa_bwd_q_kernel",
+             "bwd_fused": "fa_bwd256_kernel"}
+    kern = {}
+    for kind, lst in per_kind.items():
+        ms = statistics.mean(lst)
+        alg, exe = own[kind]
+        kern[names[kind]] = {"ms": ms, "launches": len(lst), "algorithmic_tflop": alg / 1e12,
+                             "tflops": alg / (ms / 1e3) / 1e12, "frac": alg / (ms / 1e3) / 1e12 / peak,
+                             "executed_tflops": exe / (ms / 1e3) / 1e12}
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    fwd_avg = kern["fa_fwd_kernel"]["ms"]
+    bwd_main_avg = sum(kern[n]["ms"] for n in kern if n != "fa_fwd_kernel")
     tag = f"{dom}_{profile_key}"
-    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": kern[dom]["tflops"], "peak": peak,
+                "unit": "TFLOP/s", "frac": kern[dom]["frac"], "traffic": profile_traffic(tag),
+                "peak_source": f"{peak_src} bf16 {peak_kind} ({peak_kind} peak: the timed region is "
+                               f"{timed_s:.2f} s)",
+                "frac_of_sustained": kern[dom]["tflops"] / sustained, "kernels": kern}
+    if not fwd_only:
+        pair = flops_bwd / (bwd_main_avg / 1e3) / 1e12
+        roofline["bwd_main"] = {"ms": bwd_main_avg, "tflops": pair, "frac": pair / peak,
+                                "kernels": [n for n in kern if n != "fa_fwd_kernel"]}
     fwd_tflops = flops_fwd / (fwd_avg / 1e3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profile_traffic(tag),
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
 
     # Exponentials: one per visible pair in the forward pass and the same again in
-    # the backward pass (algorithmic counts; the two-kernel backward for d = 64, 128
-    # evaluates them twice, once in each kernel).  Peak: the MUFU rate at the SM
-    # clock sampled under load.
+    # the backward pass (algorithmic counts; the backward kernels evaluate them more
+    # than once).  Peak: the MUFU rate at the SM clock sampled under load.
     clk = clocks.summary()
     sm_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
-    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if sm_mhz:
+        clk["ms_x_mhz_per_step"] = ms_per_step * sm_mhz
+    n_sms = props.multi_processor_count
     mufu_peak = MUFU_EX2_PER_CLK_PER_SM * n_sms * sm_mhz * 1e6 if sm_mhz else None
     exps = B * H * visible_pairs(w, range(w.N))
 
@@ -473,14 +576,14 @@ def main():
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
                        "step": "fwd" if fwd_only else ("fwd + bwd (pre, dK/dV kernel, dQ kernel)" if d in (64, 128)
-                                                        else "fwd + bwd (pre, main, dq convert)"),
+                                                        else "fwd + bwd (pre, one launch of dK, dV and dQ CTAs)"),
                        "l2": "256 MB flush write before every step", "parallelism": f"replicas x{world}"},
-            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / float(peaks["bf16_tflops"]),
+            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak_burst": fwd_tflops / burst,
                     **exp_rate(fwd_avg)},
             "bwd": None if fwd_only else {
                 "tflops": flops_bwd / (statistics.mean(bwd_ms) / 1e3) / 1e12, "ms": statistics.mean(bwd_ms),
-                "main_kernel_ms": bwd_main_avg,
-                "main_kernel_frac_of_peak_sustained": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / peak,
+                "main_kernels_ms": bwd_main_avg,
+                "main_kernels_frac_of_peak_burst": flops_bwd / (bwd_main_avg / 1e3) / 1e12 / burst,
                 **exp_rate(bwd_main_avg)},
             "mufu_peak_exp_per_s": mufu_peak,
             "roofline": roofline,
@@ -489,7 +592,7 @@ def main():
                     "ms_per_step": e2e_ms / K,
                     "path": f"{'fa_fwd_host' if fwd_only else 'fa_fwd_bwd_host'} (C ABI, pinned host buffers, "
                             f"{args.chunks if args.chunks > 0 else 'default'} head chunks)"},
-            "gpu_launches": (1 if fwd_only else 4) * K,
+            "gpu_launches": (1 if fwd_only else n_launch + 1) * K,  # + the D pre-pass
             "clocks": clk,
         }
         print(json.dumps(out))

@@ -235,20 +235,23 @@ def fa_selftest_wait_timeout(limit_us: int, stream=None):
     _check("fa_selftest_wait_timeout", load().fa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
+PROFILE_KINDS = {0: "fwd", 1: "bwd_kv", 2: "bwd_q", 3: "bwd_fused"}
+
+
 def fa_profile_begin(n: int):
-    """Record the main-kernel time of the next ``n`` fa_fwd / fa_bwd calls."""
+    """Record the time of each of the next ``n`` main-kernel launches of fa_fwd / fa_bwd."""
     _check("fa_profile_begin", load().fa_profile_begin(int(n)))
 
 
 def fa_profile_end(max_out: int = 65536):
-    """Wait for the recorded events; returns [(kind, ms)] in call order, kind 'fwd' or 'bwd'."""
+    """Wait for the recorded events; returns [(kind, ms)] in launch order, kind one of
+    PROFILE_KINDS' names."""
     ms = (ctypes.c_float * max_out)()
     kind = (ctypes.c_int * max_out)()
     n = load().fa_profile_end(ms, kind, max_out)
     if n < 0:
         raise FaError("fa_profile_end", 5)
-    names = {0: "fwd", 1: "bwd"}
-    return [(names.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n)]
+    return [(PROFILE_KINDS.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n)]
 
 
 def fa_status_string(code: int) -> str:

@@ -79,6 +79,8 @@ fa_status check_common(int B, int H, int H_kv, int Nq, int Nk, int d, float scal
   if (BH > (1LL << 24) || Nq > (1 << 28) || Nk > (1 << 28)) return FA_ERR_UNSUPPORTED;
   if (BH * ((Nq + 127) / 128) * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H_kv * ((Nk + 127) / 128) * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  // the d = 256 backward launches both kinds of CTA in one grid
+  if (BH * ((Nq + 127) / 128) + (long long)B * H_kv * ((Nk + 127) / 128) * 2 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   // Queries with an empty key set are not a supported problem.
   if (BH * Nq > 0 && Nk == 0) return FA_ERR_UNSUPPORTED;
   return FA_OK;
@@ -152,16 +154,9 @@ void profile_mark_end(cudaStream_t stream, int kind) {
   if (cudaEventRecord(p.ev[p.used].second, stream) == cudaSuccess) p.kind[p.used++] = kind;
 }
 
-int bwd_query_rows(int d);
-
-size_t bwd_lse_offset(long long BH, int N, int d) {
-  return bwd_needs_dq_acc(d) ? round_up((size_t)BH * N * d * sizeof(float), 256) : 0;
-}
-size_t bwd_delta_offset(long long BH, int N, int d) {
-  return bwd_lse_offset(BH, N, d) + round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256);
-}
-size_t bwd_workspace_bytes(long long BH, int N, int d) {
-  return bwd_delta_offset(BH, N, d) + round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256);
+size_t bwd_delta_offset(long long BH, int N) { return round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256); }
+size_t bwd_workspace_bytes(long long BH, int N) {
+  return bwd_delta_offset(BH, N) + round_up((size_t)BH * bwd_npad(N) * sizeof(float), 256);
 }
 
 }  // namespace fa
@@ -235,7 +230,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_common(B, H, H > 0 ? 1 : 0, N, N, d, 1.f, FA_FP16) != FA_OK) return 0;
   if ((size_t)B * H * N == 0) return 0;
-  return bwd_workspace_bytes((long long)B * H, N, d);
+  return bwd_workspace_bytes((long long)B * H, N);
 }
 
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -263,18 +258,19 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   if ((st = check_device()) != FA_OK) return st;
   const bool bf16 = dtype == FA_BF16;
   const long long BH = (long long)B * H, BHkv = (long long)B * H_kv;
-  const int bm = bwd_query_rows(d);
+  const int rows = bwd_box_rows(d);
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_map(&mq, q, BH, N_q, d, bf16, bm) || !make_map(&mk, k, BHkv, N_k, d, bf16, 128) ||
-      !make_map(&mv, v, BHkv, N_k, d, bf16, 128) || !make_map(&mdo, dout, BH, N_q, d, bf16, bm))
+  if (!make_map(&mq, q, BH, N_q, d, bf16, rows) || !make_map(&mk, k, BHkv, N_k, d, bf16, rows) ||
+      !make_map(&mv, v, BHkv, N_k, d, bf16, rows) || !make_map(&mdo, dout, BH, N_q, d, bf16, rows))
     return FA_ERR_CUDA;
   BwdArgs a{};
+  a.q = q;
+  a.k = k;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.dq_acc = bwd_needs_dq_acc(d) ? static_cast<float*>(workspace) : nullptr;
-  a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_lse_offset(BH, N_q, d));
-  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_delta_offset(BH, N_q, d));
+  a.lse_log2 = static_cast<float*>(workspace);
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_delta_offset(BH, N_q));
   a.Npad = bwd_npad(N_q);
   a.dq = dq;
   a.dk = dk;
@@ -309,9 +305,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 namespace fa {
 namespace {
 // Fixed scratch of fa_bwd_noalloc (the backward workspace: fp32 L log2 e and D
-// rows, plus the fp32 dQ accumulator for d = 256).  Its
-// name in host code is only a host-side stand-in; the device address comes
-// from cudaGetSymbolAddress on each device.
+// rows).  Its name in host code is only a host-side stand-in; the device address
+// comes from cudaGetSymbolAddress on each device.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -1,0 +1,558 @@
+// Backward pass for head dimension 256: one launch of three kinds of CTA, no
+// atomics, so dQ, dK and dV are bitwise reproducible.
+//
+// Like the d = 64 / 128 kernels it rebuilds the probabilities block by block from
+// Q, K and the forward pass's logsumexp (page "FlashAttention — فلاش أتنشن",
+// section "Tiling and block processing") and applies the chain-rule derivatives
+// of the attention formula (same page, section "The problem of standard
+// attention"):
+//
+//   P = 2^(S scale log2 e - L log2 e),   dP = dO V^T,   dS = P o (dP - D),
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
+//
+// At d = 256 a 128-row accumulator of one gradient fills half of the tensor
+// memory (256 of 512 columns) and a 128-row operand tile takes 64 KB of shared
+// memory, so dK and dV cannot both stay in one CTA next to the score tiles.  The
+// work is therefore split by output:
+//
+//   dK CTA  (key/value head, 128-key block): keys on TMEM lanes.  K is copied once
+//           into tensor memory and is the A operand of S^T = K Q^T; V stays in
+//           shared memory for dP^T = V dO^T; Q and dO stream in 64-row tiles;
+//           dK += dS^T Q with dS^T packed in tensor memory.
+//   dV CTA  (same block): K in tensor memory, S^T = K Q^T into two alternating
+//           64-column buffers, P^T packed in place, dV += P^T dO.
+//   dQ CTA  (query head, 128-row query block): queries on TMEM lanes.  Q in tensor
+//           memory is the A operand of S = Q K^T; dO stays in shared memory for
+//           dP = dO V^T; K and V stream in 64-key tiles; dQ += dS K.
+//
+// The dK and dQ CTAs run the same program on swapped operands (K, V, Q, dO) <->
+// (Q, dO, K, V), with the per-column (dK) or per-row (dQ) L and D.  The key-block
+// CTAs are the key-block parallelism of page "FlashAttention-2 — فلاش أتنشن-2",
+// section "Technical architecture", item 2; each visits the query blocks of every
+// query head of its key/value head's group, so the group sums of dK and dV stay
+// in tensor memory.  The dK and dV CTAs of one key block are adjacent in the
+// grid (they stream the same Q and dO tiles), and the dQ CTAs follow them.
+//
+// Tensor memory: columns 0-127 hold the resident operand (K or Q, 16-bit pairs),
+// 128-191 and 192-255 two 64-column score buffers (S and dP, or two S^T), 256-511
+// the gradient accumulator.  Shared memory: the stationary 128-row tile (64 KB),
+// three 64-row stages of the operand read by the score and gradient products,
+// two of the operand read by the second product (32 KB each), and the L, D
+// values of each query stage.  Warps: 0-7 elementwise (two warpgroups, 32 tile
+// columns each), 8 TMA, 9 MMA.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kRoleDK = 0, kRoleDV = 1, kRoleDQ = 2;
+constexpr int kRes = 128;                    // rows of the resident operand (= TMEM lanes)
+constexpr int kBlk = 64;                     // rows of a streamed tile
+constexpr uint32_t kP64 = 64 * 128;          // one 64-column panel of 64 rows (8 KB)
+constexpr uint32_t kP128 = 128 * 128;        // one 64-column panel of 128 rows (16 KB)
+constexpr uint32_t kT64 = 4 * kP64;          // 64 rows x 256 columns (32 KB)
+constexpr uint32_t kT128 = 4 * kP128;        // 128 rows x 256 columns (64 KB)
+constexpr int kZStages = 3, kWStages = 2;
+constexpr int kEwWarps = 8;
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 10 * 32;
+
+// shared memory
+constexpr uint32_t kSmY = 0;
+constexpr uint32_t kSmZ = kT128;
+constexpr uint32_t kSmW = kSmZ + kZStages * kT64;
+constexpr uint32_t kSmLD = kSmW + kWStages * kT64;          // per Z stage: 64 L log2 e, then 64 D
+constexpr uint32_t kSmBar = kSmLD + kZStages * 512;
+enum : int {
+  kYFull = 0,
+  kAReady = 1,                 // the resident operand is in tensor memory
+  kZFull = 2,                  // three
+  kZEmpty = kZFull + kZStages,
+  kWFull = kZEmpty + kZStages, // two
+  kWEmpty = kWFull + kWStages,
+  kSReady = kWEmpty + kWStages,  // two (the dV CTA alternates; the others use the first)
+  kSFree = kSReady + 2,        // the scores have been read out of tensor memory
+  kDpReady = kSFree + 1,
+  kDsFull = kDpReady + 1,      // dS packed into the dP buffer
+  kPFull = kDsFull + 1,        // two: P^T packed into its score buffer (dV CTA)
+  kDone = kPFull + 2,          // the last gradient product has completed
+  kNumBars
+};
+constexpr uint32_t kSmTmemSlot = kSmBar + kNumBars * 8;
+constexpr uint32_t kSmAlloc = kSmTmemSlot + 16 + 1024;  // + alignment of the dynamic base
+static_assert(kSmAlloc <= 232448, "shared memory budget");
+
+// tensor memory columns
+constexpr uint32_t kTmA = 0;
+constexpr uint32_t kTmBuf0 = 128;
+constexpr uint32_t kTmBuf1 = 192;
+constexpr uint32_t kTmG = 256;
+
+constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand: 8-row groups 1024 B apart
+constexpr uint32_t idesc_score(bool bf16) { return make_idesc_f16(bf16, 128, kBlk, false, false); }
+constexpr uint32_t idesc_grad(bool bf16) { return make_idesc_f16(bf16, 128, 256, false, true); }
+
+// Column (relative to a score buffer) of the packed 16-bit pairs of K step kk:
+// warpgroup e packs its 32 columns into the first 16 columns of its own range, so
+// no warpgroup writes where the other still reads.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return 32u * (kk >> 1) + 8u * (kk & 1); }
+
+// Acc (128 x 64) = A B^T, A the resident 128 x 256 operand in tensor memory,
+// B a 64-row K-major tile in shared memory.
+__device__ __forceinline__ void score_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc) {
+  const uint32_t b0 = sdesc_lo(b_smem, 16);
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk)
+    mma_ts_lohi(d_tmem, a_tmem + 8 * kk, b0 + (((kk >> 2) * kP64 + (kk & 3) * 32) >> 4), kHi, idesc, kk > 0);
+}
+// Acc (128 x 64) = A B^T, A a 128-row and B a 64-row K-major tile in shared memory.
+__device__ __forceinline__ void score_ss(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
+  const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, 16);
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk)
+    mma_ss_lohi(d_tmem, a0 + (((kk >> 2) * kP128 + (kk & 3) * 32) >> 4), kHi,
+                b0 + (((kk >> 2) * kP64 + (kk & 3) * 32) >> 4), kHi, idesc, kk > 0);
+}
+// Acc (128 x 256) (+)= A B, A (128 x 64) packed in a score buffer, B a 64-row tile
+// read MN-major (rows = K, four 64-column panels of N).
+__device__ __forceinline__ void grad_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc, bool acc) {
+  const uint32_t b0 = sdesc_lo(b_smem, kP64);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts_lohi(d_tmem, a_tmem + packed_col(kk), b0 + ((kk * 2048) >> 4), kHi, idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+// TMA load of a 64-row tile (four 64-column boxes) completing `bar`.
+__device__ __forceinline__ void load_tile64(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) tma_load_3d(dst + p * kP64, m, bar, 64 * p, row, plane);
+}
+// A 128-row tile as two 64-row boxes per panel (the same 128-byte-swizzled layout
+// a 128-row box gives: the second box starts 64 rows = 8 KB into the panel).
+__device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    tma_load_3d(dst + p * kP128, m, bar, 64 * p, row, plane);
+    tma_load_3d(dst + p * kP128 + kP64, m, bar, 64 * p, row + 64, plane);
+  }
+}
+
+__device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void ld_shared_f4(uint32_t addr, float4& v) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+}
+
+template <int ROLE, bool BF16>
+__device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                           const CUtensorMap* tm_do, const BwdArgs& args, int blk, int head,
+                                           uint8_t* smem, uint32_t sbase, uint32_t tmem) {
+  constexpr bool kKeyRows = ROLE != kRoleDQ;  // keys on TMEM lanes (dK, dV CTAs)
+  constexpr bool kThree = ROLE != kRoleDV;    // S, dP and the gradient product
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  auto sZ = [&](int s) -> uint32_t { return sbase + kSmZ + kT64 * s; };
+  auto sW = [&](int s) -> uint32_t { return sbase + kSmW + kT64 * s; };
+  auto sLD = [&](int s) -> uint32_t { return sbase + kSmLD + 512u * s; };
+  const uint32_t sY = sbase + kSmY;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N, Nk = args.Nk;
+  const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
+
+  // ---- this CTA's rows and the blocks it streams
+  int row0, nit, nit_h = 1, bh_q0 = 0, plane_a;
+  if constexpr (kKeyRows) {
+    row0 = blk * kRes;  // first key
+    plane_a = head;     // key/value plane
+    const int nqb = (N + kBlk - 1) / kBlk;
+    const int i_begin = args.causal ? max(0, row0 - koff) / kBlk : 0;
+    nit_h = nqb - i_begin;  // >= 1: the last query row sees every key
+    nit = nit_h * args.group;
+    const int hpb = args.H / args.group;
+    bh_q0 = (head / hpb) * args.H + (head % hpb) * args.group;
+  } else {
+    row0 = blk * kRes;  // first query
+    plane_a = head;     // query plane
+    const int last = args.causal ? min(Nk - 1, row0 + kRes - 1 + koff) : Nk - 1;  // last key any row sees
+    nit = last < 0 ? 0 : last / kBlk + 1;
+  }
+  const int i_begin = kKeyRows ? (args.causal ? max(0, row0 - koff) / kBlk : 0) : 0;
+  const int bh_kv = kKeyRows ? head : (head / args.H) * (args.H / args.group) + (head % args.H) / args.group;
+  // streamed block it: its first row and plane
+  auto z_row = [&](int it) { return kKeyRows ? (i_begin + it % nit_h) * kBlk : it * kBlk; };
+  auto z_plane = [&](int it) { return kKeyRows ? bh_q0 + it / nit_h : bh_kv; };
+  const CUtensorMap* mZ = kKeyRows ? tm_q : tm_k;
+  const CUtensorMap* mW = kKeyRows ? tm_do : tm_v;
+  const CUtensorMap* mY = kKeyRows ? tm_v : tm_do;
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nit > 0) {
+      if constexpr (kThree) {
+        mbar_expect_tx(bar(kYFull), kT128);
+        load_tile128(sY, mY, bar(kYFull), row0, kKeyRows ? bh_kv : head);
+      }
+      int n_z = 0, n_w = 0;  // loads issued
+      for (int it = 0; it < nit; ++it) {
+        const int s = it % kZStages, u = it / kZStages;
+        if (u > 0 && !mbar_wait(bar(kZEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
+        const int zr = z_row(it), zp = z_plane(it);
+        mbar_expect_tx(bar(kZFull + s), kT64 + (kKeyRows ? 512u : 0u));
+        load_tile64(sZ(s), mZ, bar(kZFull + s), zr, zp);
+        if constexpr (kKeyRows) {
+          bulk_load(sLD(s), args.lse_log2 + (size_t)zp * args.Npad + zr, 256, bar(kZFull + s));
+          bulk_load(sLD(s) + 256, args.delta + (size_t)zp * args.Npad + zr, 256, bar(kZFull + s));
+        }
+        ++n_z;
+        const int sw = it % kWStages, uw = it / kWStages;
+        if (uw > 0 && !mbar_wait(bar(kWEmpty + sw), (uw - 1) & 1, args.err, kErrTimeoutRing)) break;
+        mbar_expect_tx(bar(kWFull + sw), kT64);
+        load_tile64(sW(sw), mW, bar(kWFull + sw), zr, zp);
+        ++n_w;
+      }
+      // Every copy this thread issued lands before the CTA exits, even when the
+      // consumers gave up after a timeout elsewhere (bounded waits, abort ignored).
+      if constexpr (kThree) mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < kZStages; ++s)
+        if (n_z > s) mbar_wait(bar(kZFull + s), ((n_z - 1 - s) / kZStages) & 1, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < kWStages; ++s)
+        if (n_w > s) mbar_wait(bar(kWFull + s), ((n_w - 1 - s) / kWStages) & 1, args.err, kErrTimeoutTma, false);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nit > 0) {
+      constexpr uint32_t kIdS = idesc_score(BF16), kIdG = idesc_grad(BF16);
+      const uint32_t tA = tmem + kTmA, tB0 = tmem + kTmBuf0, tB1 = tmem + kTmBuf1, tG = tmem + kTmG;
+      auto zfull = [&](int it) { return mbar_wait(bar(kZFull + it % kZStages), (it / kZStages) & 1, args.err, kErrTimeoutTma); };
+      auto wfull = [&](int it) { return mbar_wait(bar(kWFull + it % kWStages), (it / kWStages) & 1, args.err, kErrTimeoutTma); };
+      bool ok = mbar_wait(bar(kAReady), 0, args.err, kErrTimeoutSoftmax) && zfull(0);
+      if constexpr (kThree) {
+        // Order: S(0) dP(0) | S(i+1) G(i) dP(i+1) | ...  S(i+1) follows the read-out of
+        // S(i); dP(i+1) overwrites the packed dS(i) only after G(i) has read it (one
+        // thread's tcgen05.mma operations execute in issue order).
+        if (ok) {
+          tc_fence_after();
+          score_ts(tB0, tA, sZ(0), kIdS);
+          mma_commit(bar(kSReady));
+          ok = mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma) && wfull(0);
+        }
+        if (ok) {
+          tc_fence_after();
+          score_ss(tB1, sY, sW(0), kIdS);
+          mma_commit(bar(kDpReady));
+          mma_commit(bar(kWEmpty + 0));  // W(0): read by dP(0) only
+        }
+        for (int it = 0; ok && it < nit; ++it) {
+          if (it + 1 < nit) {
+            if (!(ok = mbar_wait(bar(kSFree), it & 1, args.err, kErrTimeoutSoftmax) && zfull(it + 1))) break;
+            tc_fence_after();
+            score_ts(tB0, tA, sZ((it + 1) % kZStages), kIdS);
+            mma_commit(bar(kSReady));
+          }
+          if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
+          tc_fence_after();
+          grad_ts(tG, tB1, sZ(it % kZStages), kIdG, it > 0);
+          mma_commit(bar(kZEmpty + it % kZStages));  // Z(it): last read by G(it)
+          if (it + 1 < nit) {
+            if (!(ok = wfull(it + 1))) break;
+            tc_fence_after();
+            score_ss(tB1, sY, sW((it + 1) % kWStages), kIdS);
+            mma_commit(bar(kDpReady));
+            mma_commit(bar(kWEmpty + (it + 1) % kWStages));
+          }
+        }
+      } else {
+        // dV: S^T(0) S^T(1) | dV(i) S^T(i+2) | ...  S^T(i+2) overwrites the packed P^T(i)
+        // only after dV(i) has read it.
+        if (ok) {
+          tc_fence_after();
+          score_ts(tB0, tA, sZ(0), kIdS);
+          mma_commit(bar(kSReady + 0));
+          if (nit > 1) {
+            if ((ok = zfull(1))) {
+              tc_fence_after();
+              score_ts(tB1, tA, sZ(1), kIdS);
+              mma_commit(bar(kSReady + 1));
+            }
+          }
+        }
+        for (int it = 0; ok && it < nit; ++it) {
+          const int b = it & 1;
+          const uint32_t tBuf = b ? tB1 : tB0;
+          if (!(ok = mbar_wait(bar(kPFull + b), (it >> 1) & 1, args.err, kErrTimeoutSoftmax) && wfull(it))) break;
+          tc_fence_after();
+          grad_ts(tG, tBuf, sW(it % kWStages), kIdG, it > 0);
+          mma_commit(bar(kWEmpty + it % kWStages));  // dO(it): read by dV(it)
+          mma_commit(bar(kZEmpty + it % kZStages));  // Q(it) and its L, D: done with block it
+          if (it + 2 < nit) {
+            if (!(ok = zfull(it + 2))) break;
+            tc_fence_after();
+            score_ts(tBuf, tA, sZ((it + 2) % kZStages), kIdS);
+            mma_commit(bar(kSReady + b));
+          }
+        }
+      }
+      mma_commit(bar(kDone));  // also ends the epilogue's wait after a failure (result discarded)
+      mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warps + epilogue
+    const int e = warp >> 2;                 // warpgroup: tile columns [32 e, 32 e + 32)
+    const int r = ((warp & 3) << 5) + lane;  // TMEM lane: key row (dK, dV) or query row (dQ)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int row = row0 + r;
+    const int nrows = kKeyRows ? Nk : N;
+    const float c = args.scale_log2;
+    bool ok = nit > 0;
+    if (ok) {
+      // ---- the resident operand (K or Q) into tensor memory: this thread's row,
+      // warpgroup e's 128 of the 256 columns, as 16-bit pairs (zeros past the end)
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(kKeyRows ? args.k : args.q) +
+                            ((size_t)plane_a * nrows + row) * 256 + 128 * e;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[32];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < nrows) v = *reinterpret_cast<const uint4*>(src + 64 * h + 8 * x);
+          a[4 * x] = v.x;
+          a[4 * x + 1] = v.y;
+          a[4 * x + 2] = v.z;
+          a[4 * x + 3] = v.w;
+        }
+        tmem_st_32x32b_x32(tmem + lane_base + kTmA + 64 * e + 32 * h, a);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(bar(kAReady));
+    }
+    // per-row L log2 e and D (dQ CTA): +inf and 0 on padding rows, so P = 0 there
+    float Lr = 0.f, Dr = 0.f;
+    if constexpr (!kKeyRows) {
+      Lr = args.lse_log2[(size_t)head * args.Npad + row];
+      Dr = args.delta[(size_t)head * args.Npad + row];
+    }
+    const int cbeg = 32 * e;
+    for (int it = 0; ok && it < nit; ++it) {
+      const int c0 = z_row(it);  // first query (dK, dV) or key (dQ) of the block
+      // some visible (key, query) pair hidden in this block: causal diagonal, or (dQ)
+      // keys past N_k in the last block (their K, V rows are zero, but P would not be)
+      const bool diag = kKeyRows ? (args.causal && row0 + kRes - 1 > c0 + koff)
+                                 : ((args.causal && c0 + kBlk - 1 > row0 + koff) || c0 + kBlk > Nk);
+      float l4v[32], d4v[32];
+      if constexpr (kKeyRows) {
+        // L log2 e and D of the block's queries arrive with its Q tile
+        const int s = it % kZStages;
+        if (!(ok = warp_wait(bar(kZFull + s), (it / kZStages) & 1, args.err, kErrTimeoutTma))) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 t;
+          ld_shared_f4(sLD(s) + 4u * (cbeg + 4 * i), t);
+          l4v[4 * i] = t.x, l4v[4 * i + 1] = t.y, l4v[4 * i + 2] = t.z, l4v[4 * i + 3] = t.w;
+          if constexpr (kThree) {
+            ld_shared_f4(sLD(s) + 256u + 4u * (cbeg + 4 * i), t);
+            d4v[4 * i] = t.x, d4v[4 * i + 1] = t.y, d4v[4 * i + 2] = t.z, d4v[4 * i + 3] = t.w;
+          }
+        }
+      }
+      // ---- P = 2^(S c - L log2 e)
+      const int b = kThree ? 0 : (it & 1);
+      const uint32_t tS = tmem + lane_base + (b ? kTmBuf1 : kTmBuf0) + cbeg;
+      if (!(ok = warp_wait(bar(kSReady + b), kThree ? (it & 1) : ((it >> 1) & 1), args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld_32x32b_x32(tS, sv);
+      tmem_wait_ld();
+      reg_fence32(sv);
+      float p[32];
+#pragma unroll
+      for (int x = 0; x < 32; x += 2) {
+        float x0, x1;
+        if constexpr (kKeyRows)
+          fma2v(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), c, -l4v[x], -l4v[x + 1], x0, x1);
+        else
+          fma2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), c, -Lr, x0, x1);
+        p[x] = ex2_approx(x0);
+        p[x + 1] = ex2_approx(x1);
+      }
+      if (diag) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int col = c0 + cbeg + x;
+          const bool hidden = kKeyRows ? (args.causal && row > col + koff)
+                                       : ((args.causal && col > row + koff) || col >= Nk);
+          if (hidden) p[x] = 0.f;
+        }
+      }
+      if constexpr (!kThree) {
+        // dV CTA: P^T packed back into the first 16 columns of this warpgroup's part
+        uint32_t pw[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[2 * x], p[2 * x + 1]);
+        tmem_st_32x32b_x16(tS, pw);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(bar(kPFull + b));
+      } else {
+        tc_fence_before();
+        warp_arrive(bar(kSFree));  // the scores may be overwritten by the next block's now
+        // ---- dS = P o (dP - D), packed into the dP buffer
+        const uint32_t tDP = tmem + lane_base + kTmBuf1 + cbeg;
+        if (!(ok = warp_wait(bar(kDpReady), it & 1, args.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(tDP, dv);
+        tmem_wait_ld();
+        reg_fence32(dv);
+        uint32_t dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          float ds0, ds1;
+          if constexpr (kKeyRows)
+            submul2(p[x], p[x + 1], __uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), d4v[x], d4v[x + 1], ds0, ds1);
+          else
+            submul2(p[x], p[x + 1], __uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), Dr, Dr, ds0, ds1);
+          dw[x >> 1] = pack2<BF16>(ds0, ds1);
+        }
+        tmem_st_32x32b_x16(tDP, dw);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(bar(kDsFull));
+      }
+    }
+    // ---- the gradient rows: lane r holds row `row`; warpgroup e writes columns
+    // [128 e, 128 e + 128).  A dQ CTA whose rows see no key writes dQ = 0.
+    if (nit == 0 || (ok && warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
+      tc_fence_after();
+      const float mul = ROLE == kRoleDV ? 1.f : args.scale;
+      void* out = ROLE == kRoleDK ? args.dk : (ROLE == kRoleDV ? args.dv : args.dq);
+      uint16_t* dst = reinterpret_cast<uint16_t*>(out) + ((size_t)plane_a * nrows + row) * 256 + 128 * e;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        if (nit > 0) {
+          tmem_ld_32x32b_x32(tmem + lane_base + kTmG + 128 * e + 32 * ch, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] = 0u;
+        }
+        if (row < nrows) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8)
+            st_global_v4(dst + 32 * ch + x, pack2<BF16>(__uint_as_float(v[x]) * mul, __uint_as_float(v[x + 1]) * mul),
+                         pack2<BF16>(__uint_as_float(v[x + 2]) * mul, __uint_as_float(v[x + 3]) * mul),
+                         pack2<BF16>(__uint_as_float(v[x + 4]) * mul, __uint_as_float(v[x + 5]) * mul),
+                         pack2<BF16>(__uint_as_float(v[x + 6]) * mul, __uint_as_float(v[x + 7]) * mul));
+        }
+      }
+    }
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // CTA -> (role, block, head).  First the key-block CTAs, the dK and dV CTAs of one
+  // (key/value head, key block) side by side, lowest key blocks first (under the
+  // causal mask they see the most query blocks); then the dQ CTAs, the last query
+  // blocks first.  Heads in groups (grouped_tile) so the running CTAs' tiles stay in L2.
+  const int nkb = (args.Nk + kRes - 1) / kRes;
+  const int nqb = (args.N + kRes - 1) / kRes;
+  const unsigned n_kv = 2u * (unsigned)nkb * (unsigned)args.BHkv;
+  int role, blk, head;
+  if (blockIdx.x < n_kv) {
+    role = (blockIdx.x & 1) ? kRoleDV : kRoleDK;
+    grouped_tile(blockIdx.x >> 1, args.BHkv, nkb, args.head_group_kv, blk, head);
+  } else {
+    role = kRoleDQ;
+    grouped_tile(blockIdx.x - n_kv, args.BH, nqb, args.head_group_q, blk, head);
+    blk = nqb - 1 - blk;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(sbase + kSmBar + 8u * kYFull, 1);
+    mbar_init(sbase + kSmBar + 8u * kAReady, kEwWarps);
+    for (int s = 0; s < kZStages; ++s) {
+      mbar_init(sbase + kSmBar + 8u * (kZFull + s), 1);
+      mbar_init(sbase + kSmBar + 8u * (kZEmpty + s), 1);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(sbase + kSmBar + 8u * (kWFull + s), 1);
+      mbar_init(sbase + kSmBar + 8u * (kWEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sbase + kSmBar + 8u * (kSReady + b), 1);
+      mbar_init(sbase + kSmBar + 8u * (kPFull + b), kEwWarps);
+    }
+    mbar_init(sbase + kSmBar + 8u * kSFree, kEwWarps);
+    mbar_init(sbase + kSmBar + 8u * kDpReady, 1);
+    mbar_init(sbase + kSmBar + 8u * kDsFull, kEwWarps);
+    mbar_init(sbase + kSmBar + 8u * kDone, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(sbase + kSmTmemSlot, 512);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+
+  if (role == kRoleDK)
+    bwd256_cta<kRoleDK, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
+  else if (role == kRoleDV)
+    bwd256_cta<kRoleDV, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
+  else
+    bwd256_cta<kRoleDQ, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                       const BwdArgs& a, cudaStream_t stream) {
+  auto kern = fa_bwd256_kernel<BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmAlloc);
+  if (e != cudaSuccess) return e;
+  const long long grid = 2LL * ((a.Nk + kRes - 1) / kRes) * a.BHkv + (long long)((a.N + kRes - 1) / kRes) * a.BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  profile_mark_begin(stream);
+  kern<<<(unsigned)grid, kThreads, kSmAlloc, stream>>>(q, k, v, dout, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_mark_end(stream, kProfileBwdFused);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_256(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
+  return bf16 ? launch_256<true>(q, k, v, dout, a, stream) : launch_256<false>(q, k, v, dout, a, stream);
+}
+
+}  // namespace fa

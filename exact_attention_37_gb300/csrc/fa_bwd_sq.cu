@@ -604,7 +604,10 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     bool ok = nkv > 0;
     for (int j = 0; ok && j < nkv; ++j) {
       const int k0 = 128 * j;
-      const bool diag = args.causal && (k0 + 127 > q0 + koff);  // some key hidden from some query
+      // some key of the block hidden from some query: the causal diagonal, or keys past
+      // N_k in the last block (their K, V rows are zero-filled, but P would not be:
+      // 2^(-L) can overflow when a row's scores are all very negative)
+      const bool diag = (args.causal && k0 + 127 > q0 + koff) || k0 + 128 > Nk;
       // ---- P = 2^(S c - L log2 e), kept in registers
       if (!(ok = warp_wait(bar(kSReady), j & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
@@ -624,8 +627,10 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         }
         if (diag) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (k0 + cbeg + 32 * ch + x > q + koff) p[32 * ch + x] = 0.f;
+          for (int x = 0; x < 32; ++x) {
+            const int key = k0 + cbeg + 32 * ch + x;
+            if ((args.causal && key > q + koff) || key >= Nk) p[32 * ch + x] = 0.f;
+          }
         }
       }
       tc_fence_before();
@@ -706,9 +711,11 @@ cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensor
   profile_mark_begin(stream);
   kkv<<<(unsigned)grid_kv, kThreads, kKvSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_mark_end(stream, kProfileBwdKV);
+  profile_mark_begin(stream);
   kq<<<(unsigned)grid_q, kThreads, kQSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  profile_mark_end(stream, 1);
+  profile_mark_end(stream, kProfileBwdQ);
   return cudaSuccess;
 }
 

@@ -392,7 +392,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   kern<<<(unsigned)grid, (4 * NQ + 2) * 32, L::kAlloc, stream>>>(q, k, v, o, a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  profile_mark_end(stream, 0);
+  profile_mark_end(stream, kProfileFwd);
   return cudaSuccess;
 }
 

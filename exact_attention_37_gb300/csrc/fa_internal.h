@@ -25,10 +25,11 @@ struct FwdArgs {
 
 // Arguments of the backward kernels that are not TMA descriptors.
 struct BwdArgs {
+  const void* q;         // [B*H, N, d] queries (16-bit)
+  const void* k;         // [B*H_kv, Nk, d] keys (16-bit)
   const void* o;         // [B*H, N, d] forward output (16-bit)
   const void* dout;      // [B*H, N, d] upstream gradient (16-bit)
   const float* lse;      // [B*H, N] logsumexp from the forward pass
-  float* dq_acc;         // [B*H, N, d] fp32 dQ accumulator (workspace)
   float* lse_log2;       // [B*H, Npad] L * log2(e), +inf on padding rows (workspace)
   float* delta;          // [B*H, Npad] fp32 D = rowsum(dO o O), 0 on padding rows (workspace)
   void* dq;              // [B*H, N, d] 16-bit dQ output
@@ -66,25 +67,34 @@ int fwd_rows_per_cta(int d);
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream);
 
-// Measurement hook: events around a main kernel while profiling is on (no-ops otherwise).
+// Measurement hook: events around each main kernel launch while profiling is on
+// (no-ops otherwise).  Kinds, as fa_profile_end reports them:
+enum : int {
+  kProfileFwd = 0,       // the fused forward kernel
+  kProfileBwdKV = 1,     // the dK/dV kernel (d = 64, 128)
+  kProfileBwdQ = 2,      // the dQ kernel (d = 64, 128)
+  kProfileBwdFused = 3,  // the one backward launch of d = 256
+};
 void profile_mark_begin(cudaStream_t stream);
 void profile_mark_end(cudaStream_t stream, int kind);
 
-// Whether the backward pass for head dimension d accumulates dQ in an fp32
-// workspace buffer (reductions from every key block) or writes dQ directly.
-bool bwd_needs_dq_acc(int d);
-
-// Workspace layout of the backward pass (bytes): the dQ accumulator (if the head
-// dimension needs one), then L*log2(e) and D rows padded per head to a multiple
-// of 128, each part 256-byte aligned.
-size_t bwd_workspace_bytes(long long BH, int N, int d);
-size_t bwd_lse_offset(long long BH, int N, int d);
-size_t bwd_delta_offset(long long BH, int N, int d);
+// Workspace layout of the backward pass (bytes): L*log2(e) and D rows padded per
+// head to a multiple of 128, each part 256-byte aligned.  The same for every head
+// dimension: no kernel keeps a gradient accumulator in device memory.
+size_t bwd_workspace_bytes(long long BH, int N);
+size_t bwd_delta_offset(long long BH, int N);
 inline int bwd_npad(int N) { return (N + 127) / 128 * 128; }
+
+// Rows per TMA box of the backward pass's Q, K, V, dO descriptors for head dimension d.
+inline int bwd_box_rows(int d) { return d == 256 ? 64 : 128; }
 
 // Main kernels of the backward pass with 128 x 128 tiles (d = 64, 128): dK/dV, then dQ.
 cudaError_t launch_bwd_main_sq(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
+
+// Main kernel of the backward pass for d = 256 (dK, dV and dQ CTAs in one launch).
+cudaError_t launch_bwd_main_256(bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
 
 // Failure-detection self-test: one bounded wait that nothing completes.
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);

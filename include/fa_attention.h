@@ -91,13 +91,11 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream);
 
 /*
- * Bytes of device workspace `fa_bwd` needs: for d = 256 an fp32 dQ accumulator
- * [B,H,N,d] (that head dimension sums dQ with reductions from every key block),
- * then two fp32 row vectors (L log2 e and D = rowsum(dO o O)) whose rows are
- * padded per head to a multiple of 128, each part 256-byte aligned.  Linear in
- * N: about B*H*N*(4d + 8) bytes for d = 256, B*H*N*8 for d = 64 and 128, whose
- * dQ kernel keeps its accumulator on chip.
- * Returns 0 for invalid or empty sizes.
+ * Bytes of device workspace `fa_bwd` needs: two fp32 row vectors (L log2 e and
+ * D = rowsum(dO o O)) whose rows are padded per head to a multiple of 128, each
+ * part 256-byte aligned -- 8 bytes per (padded) query row at every head
+ * dimension, linear in N.  No kernel keeps a gradient accumulator in device
+ * memory.  Returns 0 for invalid or empty sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -115,11 +113,10 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace    : device buffer of at least fa_bwd_workspace_size(B,H,N,d)
  *                  bytes, 256-byte aligned; contents need not be initialised
  *                  and are overwritten.
- * Launches, in order on `stream`: the pre-pass (D and L log2 e; for d = 256
- * it also zeroes the dQ accumulator), then for d = 64 and 128 a
- * key-block-parallel dK/dV kernel and a query-block-parallel dQ kernel, for
- * d = 256 one key-block-parallel kernel (dK, dV, and dQ by fp32 reductions into
- * the accumulator) and the dQ conversion.
+ * Launches, in order on `stream`: the pre-pass (D and L log2 e), then for d =
+ * 64 and 128 a key-block-parallel dK/dV kernel and a query-block-parallel dQ
+ * kernel, for d = 256 one kernel whose CTAs compute dK (per key block), dV (per
+ * key block) or dQ (per query block).  No kernel uses atomics.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
@@ -132,11 +129,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * per key block, without atomics on dK/dV).  The workspace is
  * fa_bwd_workspace_size(B, H, N_q, d) bytes.  With B*H*N_q == 0 no query
  * row exists, so dk and dv are set to zero (cudaMemsetAsync on `stream`).
- * dK and dV are deterministic (one CTA sums each key row in a fixed order).
- * For d = 64 and 128 dQ is deterministic too (one CTA sums each query row over
- * the key blocks in a fixed order): repeated calls give bitwise equal
- * gradients.  For d = 256 dQ accumulates fp32 reductions from every key block,
- * so its last bits depend on scheduling.
+ * The result is deterministic at every head dimension: one CTA sums each key
+ * row of dK, dV and each query row of dQ in a fixed order, so repeated calls
+ * give bitwise equal gradients.
  * fa_bwd(..., N, ...) is fa_bwd_ex with H_kv = H and N_q = N_k = N.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -152,23 +147,26 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * counterpart to this entry point; it only changes where the scratch lives.)
  *
  * Arguments, layout, results and errors are those of fa_bwd, minus the
- * workspace pair.  The scratch (the fp32 row vectors and, for d = 256, the fp32
- * dQ accumulator: fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
+ * workspace pair.  The scratch (the fp32 row vectors L log2 e and D:
+ * fa_bwd_workspace_size(B,H,N,d) bytes) lives in one fixed 32 MiB array in the
  * library's device memory, allocated when the library's device code is loaded
  * and held by every GPU that loads it until the process exits.  Calls whose
  * scratch would exceed 32 MiB (33554432 bytes) return FA_ERR_WORKSPACE and
- * launch nothing; with B*H = 1 that is N up to 32,513 rows at d = 256 and
- * 4,194,304 rows at d = 64 and 128.
+ * launch nothing: B*H*Npad <= 4,194,304, Npad being N rounded up to a multiple
+ * of 128 (with B*H = 1, N up to 4,194,304 rows).
  *
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.  No
- * call allocates: no cudaMalloc, cudaFree or allocating library routine.  Every
- * call overwrites the whole scratch region it uses before reading it (the D
- * pre-pass writes every row vector and, for d = 256, zeroes the dQ
- * accumulator), so stale contents from an earlier call
- * never leak into a result.  All calls share the one array: two calls whose
- * kernels overlap on the GPU (different streams, no ordering between them)
- * race on it and give wrong gradients; order them on one stream or with events.
+ * that device current) and caches it for the process; make that first call
+ * before any stream capture.  cudaDeviceReset (or anything else that destroys
+ * the device's primary context) invalidates the cached address, as it does the
+ * library's device error record: do not call the library on that device again
+ * in the same process.  No call allocates: no cudaMalloc, cudaFree or
+ * allocating library routine.  Every call overwrites the whole scratch region
+ * it uses before reading it (the D pre-pass writes every row vector, padding
+ * rows included), so stale contents from an earlier call never leak into a
+ * result.  All calls share the one array: two calls whose kernels overlap on
+ * the GPU (different streams, no ordering between them) race on it and give
+ * wrong gradients; order them on one stream or with events.
  */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
@@ -270,15 +268,16 @@ uint32_t fa_last_device_error_bits(void);
 void fa_last_device_error_detail(uint32_t* out4);
 
 /*
- * Measurement hook.  fa_profile_begin(n) makes the next n calls of fa_fwd and
- * fa_bwd record a pair of CUDA events (created and owned by the library) on
- * their stream around their main kernels -- the fused forward kernel, or the
- * backward main kernels (for d = 64 and 128 the dK/dV kernel and the dQ
- * kernel, for d = 256 the key-block kernel) without the pre-pass and dQ
- * conversion.
- * fa_profile_end waits for those events, writes each kernel's time in
- * milliseconds to out_ms[i] and its kind to out_kind[i] (0 forward, 1 backward),
- * in call order, stops recording and returns the number of entries written (at
+ * Measurement hook.  fa_profile_begin(n) makes the library record a pair of CUDA
+ * events (created and owned by the library) on the launching stream around each
+ * of the next n main-kernel launches of fa_fwd / fa_bwd (and their _ex forms):
+ * the fused forward kernel, and the backward kernels without the D pre-pass.
+ * One fa_fwd call makes one launch; one fa_bwd call makes two for d = 64 and
+ * 128 (the dK/dV kernel, then the dQ kernel) and one for d = 256.
+ * fa_profile_end waits for those events, writes each launch's time in
+ * milliseconds to out_ms[i] and its kind to out_kind[i] (0 forward kernel, 1
+ * dK/dV kernel, 2 dQ kernel, 3 the single backward launch of d = 256), in
+ * launch order, stops recording and returns the number of entries written (at
  * most max_out), or -1 if the events could not be read.  Returns of
  * fa_profile_begin: FA_OK, FA_ERR_INVALID_ARG (n < 0 or n > 65536), FA_ERR_CUDA
  * (event creation failed).  Not thread-safe: one recording per process.

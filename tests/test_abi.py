@@ -108,25 +108,27 @@ def test_bwd_rejects_bad_arguments_on_the_host(lib):
 def test_noalloc_backward_rejects_oversized_problems_on_the_host(lib):
     vp = ctypes.c_void_p
     args = [vp(256)] * 9
-    # the fixed scratch holds 32 MiB: d = 256 fits 32,513 rows, not 32,514
-    assert lib.fa_bwd_noalloc(*args, 1, 1, 32514, 256, 0.1, 0, 1, None) == 4
-    # d = 64, 128 keep no dQ accumulator: 8 bytes per (padded) row, 4,194,304 rows
-    assert lib.fa_bwd_noalloc(*args, 1, 1, 4194304 + 1, 128, 0.1, 0, 1, None) == 4
-    assert lib.fa_bwd_noalloc(*args, 1, 1, 4194304 + 1, 64, 0.1, 0, 1, None) == 4
+    # The fixed scratch holds 32 MiB and the workspace is 8 bytes per (padded) row at
+    # every head dimension: 4,194,304 rows fit exactly, one more does not.
+    for d in (64, 128, 256):
+        assert lib.fa_bwd_workspace_size(1, 1, 4194304, d) == 33554432
+        assert lib.fa_bwd_workspace_size(1, 1, 4194304 + 1, d) > 33554432
+        assert lib.fa_bwd_noalloc(*args, 1, 1, 4194304 + 1, d, 0.1, 0, 1, None) == 4
+        assert lib.fa_bwd_noalloc(*args, 2, 2, 1048577, d, 0.1, 0, 1, None) == 4
     assert lib.fa_bwd_noalloc(*args, 1, 1, 8, 96, 0.1, 0, 1, None) == 2
     assert lib.fa_bwd_noalloc(*args, 0, 1, 8, 64, 0.1, 0, 1, None) == 0
 
 
 def test_workspace_is_linear_in_n(lib):
-    for d, per_row in ((64, 2 * 4), (256, (256 + 2) * 4), (128, 2 * 4)):
-        # fp32 dQ accumulator row (d = 256), plus L log2 e and D
+    for d in (64, 128, 256):
+        # L log2 e and D, fp32, for every row: no kernel keeps a gradient accumulator
         sizes = [lib.fa_bwd_workspace_size(2, 16, n, d) for n in (1024, 2048, 4096, 8192)]
         for n, s in zip((1024, 2048, 4096, 8192), sizes):
-            assert 2 * 16 * n * per_row <= s <= 2 * 16 * n * per_row + 768
-    # L and D rows are padded per head to a multiple of 128
-    assert lib.fa_bwd_workspace_size(1, 1, 1, 256) == 1024 + 2 * 512
-    assert lib.fa_bwd_workspace_size(1, 1, 1, 64) == 2 * 512
-    assert lib.fa_bwd_workspace_size(1, 1, 1, 128) == 2 * 512
+            assert s == 2 * 16 * n * 2 * 4
+    # L and D rows are padded per head to a multiple of 128, each part 256-byte aligned
+    for d in (64, 128, 256):
+        assert lib.fa_bwd_workspace_size(1, 1, 1, d) == 2 * 512
+        assert lib.fa_bwd_workspace_size(3, 1, 129, d) == 2 * 3 * 256 * 4
     assert lib.fa_bwd_workspace_size(1, 1, 0, 64) == 0
     assert lib.fa_bwd_workspace_size(1, 1, 8, 96) == 0
 

@@ -1,6 +1,6 @@
-"""Bitwise repeatability of the d = 64 and d = 128 backward pass (dK/dV kernel
-plus dQ kernel, no atomics): repeated calls on the same inputs give identical
-dQ, dK, dV.
+"""Bitwise repeatability of the backward pass at every head dimension (no atomics:
+each gradient row is summed in a fixed order inside one CTA): repeated calls on
+the same inputs give identical dQ, dK, dV.
 """
 import pytest
 import torch
@@ -27,6 +27,9 @@ def built():
         Workload("det_gqa_unequal", 1, 4, 700, 128, "fp16", True, 1.0, (509, 510, 511, 512), True, 2, 1000),
         Workload("det_d64", 2, 3, 900, 64, "fp16", True, 1.0, (513, 514, 515, 516)),
         Workload("det_d64_mqa", 1, 4, 500, 64, "bf16", False, 1.0, (517, 518, 519, 520), True, 1, 777),
+        Workload("det_d256", 2, 3, 1000, 256, "bf16", False, 1.0, (521, 522, 523, 524)),
+        Workload("det_d256_causal", 2, 3, 1000, 256, "bf16", True, 1.0, (525, 526, 527, 528)),
+        Workload("det_d256_gqa_unequal", 1, 4, 700, 256, "fp16", True, 1.0, (529, 530, 531, 532), True, 2, 1000),
     ],
     ids=lambda w: w.name,
 )

@@ -1,0 +1,63 @@
+"""Degenerate inputs on the GPU, against the fp64 oracle.
+
+Rows whose scores are all very negative: the logsumexp L of such a row is far
+below zero, so 2^(S c - L log2 e) for a key whose score is zero (a zero-filled
+key row past N_k in a ragged last block) would overflow.  Those keys are not
+part of the problem and must contribute nothing, not inf or NaN.  The inputs
+are seeded: K rows are all close to one direction u and some query rows point
+the other way, so their scores sit near -120.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_37_gb300 as fa
+import oracle
+from exact_attention_37_gb300.synth import DTYPES
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from exact_attention_37_gb300 import build
+
+    build.build()
+    fa.load()
+
+
+def very_negative_rows(H, N, Nk, d, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    u = torch.ones(d)
+    k = u + 0.05 * torch.randn(1, H, Nk, d, generator=g)
+    q = torch.randn(1, H, N, d, generator=g)
+    # scale * q.k = -(120 / sqrt(d)) * |u|^2 / sqrt(d) = -120 for the planted rows
+    q[:, :, ::3] = -(120.0 / d ** 0.5) * u + 0.05 * torch.randn(1, H, (N + 2) // 3, d, generator=g)
+    v = torch.randn(1, H, Nk, d, generator=g)
+    do = torch.randn(1, H, N, d, generator=g)
+    return tuple(x.to(DTYPES[dtype]) for x in (q, k, v, do))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Nk", [200, 333])
+def test_rows_with_very_negative_scores_and_a_ragged_key_tail(d, Nk):
+    N = 150
+    q, k, v, do = very_negative_rows(2, N, Nk, d, "bf16", 600 + d + Nk)
+    scale = float(np.float32(1.0 / np.sqrt(d)))  # the fp32 value the kernels receive
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, scale=scale, causal=False)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, scale=scale, causal=False)
+    fa.fa_check_device_status()
+    O_ref, L_ref = oracle.attention_forward(q, k, v, scale, False)
+    assert L_ref[0, 0, 0] < -100  # the planted rows really are far below zero: e^-L overflows fp32
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    O = parity.to_np(o)
+    assert np.abs(O - O_ref).max() <= parity.O_ABS["bf16"]
+    parity.compare_l(lse.cpu().numpy().astype(np.float64), L_ref)
+    rdq, rdk, rdv, _ = oracle.attention_backward(q, k, v, do, scale, False)
+    parity.compare_g(parity.to_np(dq), rdq, "dQ")
+    parity.compare_g(parity.to_np(dk), rdk, "dK")
+    parity.compare_g(parity.to_np(dv), rdv, "dV")
