@@ -22,6 +22,7 @@ STATUS = {
     4: "FA_ERR_WORKSPACE",
     5: "FA_ERR_CUDA",
     6: "FA_ERR_DEVICE_TIMEOUT",
+    7: "FA_ERR_DEVICE_CHECK",
 }
 FA_FP16, FA_BF16 = 0, 1
 
@@ -43,6 +44,7 @@ SIGNATURES = {
                              _vp]),
     "fa_check_device_status": (_i, [_vp]),
     "fa_selftest_wait_timeout": (_i, [ctypes.c_uint32, _vp]),
+    "fa_selftest_device_check": (_i, [_i, _vp]),
     "fa_last_device_error_bits": (ctypes.c_uint32, []),
     "fa_last_device_error_detail": (None, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
@@ -63,11 +65,8 @@ class FaError(RuntimeError):
 _lib = None
 
 
-def load(path: str = LIB_PATH):
-    """Load the shared library (once) and declare its signatures.  Raises if it is missing."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def open_library(path: str):
+    """Open a build of the library at ``path`` and declare its signatures (no caching)."""
     if not os.path.exists(path):
         raise FaError(f"loading {os.path.basename(path)} (not built; run exact_attention_37_gb300.build)", -1)
     lib = ctypes.CDLL(path)
@@ -75,8 +74,15 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (once) and declare its signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(path)
+    return _lib
 
 
 def _check(where: str, code: int):

@@ -2,7 +2,7 @@
 
 Each translation unit is compiled in parallel, then linked into one shared
 object next to this file.  A rebuild happens when a source or header is newer
-than the library.  Usage: ``python -m exact_attention_37_gb300.build [-v]``.
+than the library.  Usage: ``python -m exact_attention_37_gb300.build [-v] [-f] [--debug]``.
 """
 from __future__ import annotations
 
@@ -18,6 +18,10 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfa_attention.so")
 OBJDIR = os.path.join(HERE, "_build")
+# The debug build: the same sources with -DFA_DEBUG (device-side bounds, alignment
+# and barrier-phase checks that record into the device error record, never trap).
+LIB_DEBUG = os.path.join(HERE, "libfa_attention_debug.so")
+OBJDIR_DEBUG = os.path.join(HERE, "_build_debug")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_sq.cu", "fa_bwd256.cu", "fa_selftest.cu", "fa_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE]
@@ -36,22 +40,25 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    """Compile and link the library if needed; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link the library if needed; returns its path.  ``debug`` builds
+    the checked variant (``libfa_attention_debug.so``) instead."""
+    lib, objdir = (LIB_DEBUG, OBJDIR_DEBUG) if debug else (LIB, OBJDIR)
+    extra_flags = (*extra_flags, "-DFA_DEBUG") if debug else tuple(extra_flags)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -68,14 +75,14 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
             errors.append(f"{src}:\n{r.stderr}")
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

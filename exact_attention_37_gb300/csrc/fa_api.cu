@@ -14,6 +14,7 @@
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -357,9 +358,26 @@ fa_status fa_check_device_status(fa_stream_t stream) {
   if (rec[0] != 0) {
     const uint32_t zero[4] = {0, 0, 0, 0};
     if (cudaMemcpyToSymbol(g_error_word, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_DEVICE_TIMEOUT;
+    // the first failure decides: a debug-build check (code kDbgBase | kind) or a wait
+    return (rec[1] & kDbgBase) ? FA_ERR_DEVICE_CHECK : FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;
+}
+
+fa_status fa_selftest_device_check(int kind, fa_stream_t stream) {
+#ifdef FA_DEBUG
+  if (kind < (int)kDbgTmaCol || kind > (int)kDbgPhase) return FA_ERR_INVALID_ARG;
+  fa_status st = check_device();
+  if (st != FA_OK) return st;
+  uint32_t* err = error_word_ptr();
+  if (!err) return FA_ERR_CUDA;
+  return launch_selftest_check(err, kind, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                  : FA_ERR_CUDA;
+#else
+  (void)kind;
+  (void)stream;
+  return FA_ERR_UNSUPPORTED;  // the checks are compiled out of this build
+#endif
 }
 
 fa_status fa_selftest_wait_timeout(uint32_t limit_us, fa_stream_t stream) {
@@ -389,6 +407,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK";
   }
   return "FA_ERR_UNKNOWN";
 }

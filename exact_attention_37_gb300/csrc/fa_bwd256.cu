@@ -124,17 +124,19 @@ __device__ __forceinline__ void grad_ts(uint32_t d_tmem, uint32_t a_tmem, uint32
 }
 
 // TMA load of a 64-row tile (four 64-column boxes) completing `bar`.
-__device__ __forceinline__ void load_tile64(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+__device__ __forceinline__ void load_tile64(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane,
+                                            const Extent3& ext, uint32_t* err) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p) tma_load_3d(dst + p * kP64, m, bar, 64 * p, row, plane);
+  for (int p = 0; p < 4; ++p) tma_load_box(dst + p * kP64, m, bar, 64 * p, row, plane, ext, err);
 }
 // A 128-row tile as two 64-row boxes per panel (the same 128-byte-swizzled layout
 // a 128-row box gives: the second box starts 64 rows = 8 KB into the panel).
-__device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+__device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane,
+                                             const Extent3& ext, uint32_t* err) {
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    tma_load_3d(dst + p * kP128, m, bar, 64 * p, row, plane);
-    tma_load_3d(dst + p * kP128 + kP64, m, bar, 64 * p, row + 64, plane);
+    tma_load_box(dst + p * kP128, m, bar, 64 * p, row, plane, ext, err);
+    tma_load_box(dst + p * kP128 + kP64, m, bar, 64 * p, row + 64, plane, ext, err);
   }
 }
 
@@ -143,6 +145,20 @@ __device__ __forceinline__ void st_global_v4(void* addr, uint32_t a, uint32_t b,
 }
 __device__ __forceinline__ void ld_shared_f4(uint32_t addr, float4& v) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+}
+
+// First 64-row query block a key block starting at key0 sees (all of them without
+// the causal mask).  The last query row sees every key, so it is always a block.
+__device__ __forceinline__ int first_qblock(const BwdArgs& a, int key0) {
+  return a.causal ? max(0, key0 - (a.Nk - a.N)) / kBlk : 0;
+}
+// Blocks a CTA streams: for a dK or dV CTA the 64-row query blocks from its first
+// visible one, over every query head of its group; for a dQ CTA the 64-key blocks
+// its rows see (0 when none: then it writes dQ = 0).
+__device__ __forceinline__ int cta_blocks(const BwdArgs& a, int role, int blk) {
+  if (role != kRoleDQ) return ((a.N + kBlk - 1) / kBlk - first_qblock(a, blk * kRes)) * a.group;
+  const int last = a.causal ? min(a.Nk - 1, blk * kRes + kRes - 1 + (a.Nk - a.N)) : a.Nk - 1;  // last key any row sees
+  return last < 0 ? 0 : last / kBlk + 1;
 }
 
 template <int ROLE, bool BF16>
@@ -162,23 +178,13 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
   const int koff = Nk - N;  // key j visible to query i iff j <= i + koff
 
   // ---- this CTA's rows and the blocks it streams
-  int row0, nit, nit_h = 1, bh_q0 = 0, plane_a;
-  if constexpr (kKeyRows) {
-    row0 = blk * kRes;  // first key
-    plane_a = head;     // key/value plane
-    const int nqb = (N + kBlk - 1) / kBlk;
-    const int i_begin = args.causal ? max(0, row0 - koff) / kBlk : 0;
-    nit_h = nqb - i_begin;  // >= 1: the last query row sees every key
-    nit = nit_h * args.group;
-    const int hpb = args.H / args.group;
-    bh_q0 = (head / hpb) * args.H + (head % hpb) * args.group;
-  } else {
-    row0 = blk * kRes;  // first query
-    plane_a = head;     // query plane
-    const int last = args.causal ? min(Nk - 1, row0 + kRes - 1 + koff) : Nk - 1;  // last key any row sees
-    nit = last < 0 ? 0 : last / kBlk + 1;
-  }
-  const int i_begin = kKeyRows ? (args.causal ? max(0, row0 - koff) / kBlk : 0) : 0;
+  const int row0 = blk * kRes;  // first key (dK, dV) or query (dQ)
+  const int plane_a = head;     // key/value plane (dK, dV) or query plane (dQ)
+  const int nit = cta_blocks(args, ROLE, blk);
+  const int i_begin = kKeyRows ? first_qblock(args, row0) : 0;
+  const int nit_h = kKeyRows ? (N + kBlk - 1) / kBlk - i_begin : 1;  // query blocks per query head (>= 1)
+  const int hpb = args.H / args.group;                               // key/value heads per batch entry
+  const int bh_q0 = kKeyRows ? (head / hpb) * args.H + (head % hpb) * args.group : 0;  // first query head of the group
   const int bh_kv = kKeyRows ? head : (head / args.H) * (args.H / args.group) + (head % args.H) / args.group;
   // streamed block it: its first row and plane
   auto z_row = [&](int it) { return kKeyRows ? (i_begin + it % nit_h) * kBlk : it * kBlk; };
@@ -186,13 +192,16 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
   const CUtensorMap* mZ = kKeyRows ? tm_q : tm_k;
   const CUtensorMap* mW = kKeyRows ? tm_do : tm_v;
   const CUtensorMap* mY = kKeyRows ? tm_v : tm_do;
+  const Extent3 ext_q{256, N, args.BH}, ext_kv{256, Nk, args.BHkv};
+  const Extent3& ext_zw = kKeyRows ? ext_q : ext_kv;  // streamed tiles
+  const Extent3& ext_y = kKeyRows ? ext_kv : ext_q;   // the stationary tile
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nit > 0) {
       if constexpr (kThree) {
         mbar_expect_tx(bar(kYFull), kT128);
-        load_tile128(sY, mY, bar(kYFull), row0, kKeyRows ? bh_kv : head);
+        load_tile128(sY, mY, bar(kYFull), row0, kKeyRows ? bh_kv : head, ext_y, args.err);
       }
       int n_z = 0, n_w = 0;  // loads issued
       for (int it = 0; it < nit; ++it) {
@@ -200,16 +209,17 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
         if (u > 0 && !mbar_wait(bar(kZEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         const int zr = z_row(it), zp = z_plane(it);
         mbar_expect_tx(bar(kZFull + s), kT64 + (kKeyRows ? 512u : 0u));
-        load_tile64(sZ(s), mZ, bar(kZFull + s), zr, zp);
+        load_tile64(sZ(s), mZ, bar(kZFull + s), zr, zp, ext_zw, args.err);
         if constexpr (kKeyRows) {
-          bulk_load(sLD(s), args.lse_log2 + (size_t)zp * args.Npad + zr, 256, bar(kZFull + s));
-          bulk_load(sLD(s) + 256, args.delta + (size_t)zp * args.Npad + zr, 256, bar(kZFull + s));
+          const long long nrows = (long long)args.BH * args.Npad, first = (long long)zp * args.Npad + zr;
+          bulk_load_rows(sLD(s), args.lse_log2, first, 256, nrows, bar(kZFull + s), args.err);
+          bulk_load_rows(sLD(s) + 256, args.delta, first, 256, nrows, bar(kZFull + s), args.err);
         }
         ++n_z;
         const int sw = it % kWStages, uw = it / kWStages;
         if (uw > 0 && !mbar_wait(bar(kWEmpty + sw), (uw - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kWFull + sw), kT64);
-        load_tile64(sW(sw), mW, bar(kWFull + sw), zr, zp);
+        load_tile64(sW(sw), mW, bar(kWFull + sw), zr, zp, ext_zw, args.err);
         ++n_w;
       }
       // Every copy this thread issued lands before the CTA exits, even when the
@@ -454,6 +464,32 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
   }
 }
 
+// FA_DEBUG builds: the phases every barrier of a CTA completed, against its
+// protocol (thread 0, after the CTA's final barrier, when no wait gave up).
+template <int ROLE>
+__device__ __forceinline__ void check_phases(uint32_t sbase, int nit, uint32_t* err) {
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  check_phase(bar(kYFull), ROLE != kRoleDV && nit > 0, err, kYFull);
+  check_phase(bar(kAReady), nit > 0, err, kAReady);
+  for (int s = 0; s < kZStages; ++s) {
+    check_phase(bar(kZFull + s), count_mod(nit, s, kZStages), err, kZFull + s);
+    check_phase(bar(kZEmpty + s), count_mod(nit, s, kZStages), err, kZEmpty + s);
+  }
+  for (int s = 0; s < kWStages; ++s) {
+    check_phase(bar(kWFull + s), count_mod(nit, s, kWStages), err, kWFull + s);
+    check_phase(bar(kWEmpty + s), count_mod(nit, s, kWStages), err, kWEmpty + s);
+  }
+  if (ROLE == kRoleDV) {
+    for (int b = 0; b < 2; ++b) {
+      check_phase(bar(kSReady + b), count_mod(nit, b, 2), err, kSReady + b);
+      check_phase(bar(kPFull + b), count_mod(nit, b, 2), err, kPFull + b);
+    }
+  } else {
+    for (int b : {kSReady, kSFree, kDpReady, kDsFull}) check_phase(bar(b), nit, err, b);
+  }
+  check_phase(bar(kDone), nit > 0, err, kDone);
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -517,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+  debug_context(tmem, args.err);
 
   if (role == kRoleDK)
     bwd256_cta<kRoleDK, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
@@ -527,6 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kDebug) {
+    if (threadIdx.x == 0 && no_abort(args.err)) {
+      const int nit = cta_blocks(args, role, blk);
+      if (role == kRoleDK) check_phases<kRoleDK>(sbase, nit, args.err);
+      else if (role == kRoleDV) check_phases<kRoleDV>(sbase, nit, args.err);
+      else check_phases<kRoleDQ>(sbase, nit, args.err);
+    }
+  }
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -94,9 +94,10 @@ __device__ __forceinline__ void mma_packed(uint32_t d_tmem, uint32_t a_tmem, uin
 
 // TMA load of one 128-row tile (D / 64 boxes of 64 columns) completing `bar`.
 template <int D>
-__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane) {
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row, int plane,
+                                          const Extent3& ext, uint32_t* err) {
 #pragma unroll
-  for (int p = 0; p < D / 64; ++p) tma_load_3d(dst + p * kPanel, m, bar, 64 * p, row, plane);
+  for (int p = 0; p < D / 64; ++p) tma_load_box(dst + p * kPanel, m, bar, 64 * p, row, plane, ext, err);
 }
 
 // Stores 32 fp32 values (times mul) as 16-bit to dst (64 contiguous bytes).
@@ -217,13 +218,15 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+  debug_context(tmem, args.err);
+  const Extent3 ext_q{D, N, args.BH}, ext_kv{D, Nk, args.BHkv};
 
   if (warp == C::kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(bar(kKVFull), 2 * kTile);
-      load_tile<D>(sK, &tm_k, bar(kKVFull), key0, bh_kv);
-      load_tile<D>(sV, &tm_v, bar(kKVFull), key0, bh_kv);
+      load_tile<D>(sK, &tm_k, bar(kKVFull), key0, bh_kv, ext_kv, args.err);
+      load_tile<D>(sV, &tm_v, bar(kKVFull), key0, bh_kv, ext_kv, args.err);
       int n_do = 0, n_q = 0;  // loads issued
       for (int it = 0; it < nit; ++it) {
         const int s = it & 1, u = it >> 1;
@@ -231,13 +234,14 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
         // Q first: S^T of a block is issued before its dP^T.
         if (u > 0 && !mbar_wait(bar(kQEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kQFull + s), kTile + 1024);
-        load_tile<D>(sQ(s), &tm_q, bar(kQFull + s), q0, bq);
-        bulk_load(sLD(s), args.lse_log2 + (size_t)bq * args.Npad + q0, 512, bar(kQFull + s));
-        bulk_load(sLD(s) + 512, args.delta + (size_t)bq * args.Npad + q0, 512, bar(kQFull + s));
+        load_tile<D>(sQ(s), &tm_q, bar(kQFull + s), q0, bq, ext_q, args.err);
+        const long long nrows = (long long)args.BH * args.Npad, first = (long long)bq * args.Npad + q0;
+        bulk_load_rows(sLD(s), args.lse_log2, first, 512, nrows, bar(kQFull + s), args.err);
+        bulk_load_rows(sLD(s) + 512, args.delta, first, 512, nrows, bar(kQFull + s), args.err);
         ++n_q;
         if (u > 0 && !mbar_wait(bar(kDOEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kDOFull + s), kTile);
-        load_tile<D>(sDO(s), &tm_do, bar(kDOFull + s), q0, bq);
+        load_tile<D>(sDO(s), &tm_do, bar(kDOFull + s), q0, bq, ext_q, args.err);
         ++n_do;
       }
       // Every copy this thread issued lands before the CTA exits, even when the
@@ -411,6 +415,15 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kDebug) {
+    if (threadIdx.x == 0 && no_abort(args.err)) {
+      check_phase(bar(kKVFull), 1, args.err, kKVFull);
+      for (int s = 0; s < 2; ++s)
+        for (int b : {kQFull, kQEmpty, kDOFull, kDOEmpty}) check_phase(bar(b + s), count_mod(nit, s, 2), args.err, b + s);
+      for (int b : {kSReady, kPFull, kDpReady, kDsFull}) check_phase(bar(b), nit, args.err, b);
+      check_phase(bar(kDone), 1, args.err, kDone);
+    }
+  }
   if (warp == C::kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -525,23 +538,25 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+  debug_context(tmem, args.err);
+  const Extent3 ext_q{D, N, args.BH}, ext_kv{D, Nk, args.BHkv};
 
   if (warp == C::kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nkv > 0) {
       mbar_expect_tx(bar(kQFull), 2 * kTile);
-      load_tile<D>(sQ, &tm_q, bar(kQFull), q0, bh);
-      load_tile<D>(sDO, &tm_do, bar(kQFull), q0, bh);
+      load_tile<D>(sQ, &tm_q, bar(kQFull), q0, bh, ext_q, args.err);
+      load_tile<D>(sDO, &tm_do, bar(kQFull), q0, bh, ext_q, args.err);
       int n_k = 0, n_v = 0;  // loads issued
       for (int j = 0; j < nkv; ++j) {
         const int sk = j % 3, uk = j / 3, sv = j & 1, uv = j >> 1;
         if (uk > 0 && !mbar_wait(bar(kKEmpty + sk), (uk - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kKFull + sk), kTile);
-        load_tile<D>(sK(sk), &tm_k, bar(kKFull + sk), 128 * j, bh_kv);
+        load_tile<D>(sK(sk), &tm_k, bar(kKFull + sk), 128 * j, bh_kv, ext_kv, args.err);
         ++n_k;
         if (uv > 0 && !mbar_wait(bar(kVEmpty + sv), (uv - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(kVFull + sv), kTile);
-        load_tile<D>(sV(sv), &tm_v, bar(kVFull + sv), 128 * j, bh_kv);
+        load_tile<D>(sV(sv), &tm_v, bar(kVFull + sv), 128 * j, bh_kv, ext_kv, args.err);
         ++n_v;
       }
       // Every copy this thread issued lands before the CTA exits.
@@ -684,6 +699,20 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kDebug) {
+    if (threadIdx.x == 0 && no_abort(args.err)) {
+      check_phase(bar(kQFull), nkv > 0, args.err, kQFull);
+      for (int s = 0; s < 3; ++s) {
+        check_phase(bar(kKFull + s), count_mod(nkv, s, 3), args.err, kKFull + s);
+        check_phase(bar(kKEmpty + s), count_mod(nkv, s, 3), args.err, kKEmpty + s);
+      }
+      for (int s = 0; s < 2; ++s)
+        for (int b : {kVFull, kVEmpty, kDpReady, kDsFull}) check_phase(bar(b + s), count_mod(nkv, s, 2), args.err, b + s);
+      check_phase(bar(kSReady), nkv, args.err, kSReady);
+      check_phase(bar(kPDone), nkv, args.err, kPDone);
+      check_phase(bar(kDone), nkv > 0, args.err, kDone);
+    }
+  }
   if (warp == C::kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

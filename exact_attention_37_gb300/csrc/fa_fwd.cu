@@ -51,23 +51,27 @@ struct FwdLayout {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kRing = kQ + NQ * kTileBytes;
   static constexpr uint32_t kBar = kRing + STAGES * kTileBytes;
+  // One sub-tile (NQ = 1) keeps two score buffers, used by alternate key blocks, so
+  // the scores of block j+1 are computed while the softmax works on block j.
+  static constexpr int kSBufs = NQ == 1 ? 2 : NQ;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kFull = 1;
   static constexpr int kEmpty = kFull + STAGES;
-  static constexpr int kSFull = kEmpty + STAGES;
-  static constexpr int kPFull = kSFull + NQ;
-  static constexpr int kODone = kPFull + NQ;
+  static constexpr int kSFull = kEmpty + STAGES;  // one per score buffer
+  static constexpr int kPFull = kSFull + kSBufs;  // one per score buffer
+  static constexpr int kODone = kPFull + kSBufs;  // one per sub-tile
   static constexpr int kDrain = kODone + NQ;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024 B
-  // TMEM columns: S_t (P_t in its first 64 columns) at 128*t, O_t after all S tiles.
+  // TMEM columns: score buffer b (P in its first 64 columns) at 128*b, O_t after all
+  // score buffers.  With NQ = 2 sub-tile t owns buffer t.
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t s_col(int t) { return 128u * t; }
-  static constexpr uint32_t o_col(int t) { return 128u * NQ + (uint32_t)D * t; }
-  static_assert(128 * NQ + D * NQ <= 512, "TMEM budget");
+  static constexpr uint32_t s_col(int b) { return 128u * b; }
+  static constexpr uint32_t o_col(int t) { return 128u * kSBufs + (uint32_t)D * t; }
+  static_assert(128 * kSBufs + D * NQ <= 512, "TMEM budget");
   static_assert(kBytes + 1024 <= 232448, "shared memory budget");
 };
 
@@ -120,11 +124,11 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       mbar_init(bar(L::kFull + s), 1);
       mbar_init(bar(L::kEmpty + s), 1);
     }
-    for (int t = 0; t < NQ; ++t) {
-      mbar_init(bar(L::kSFull + t), 1);
-      mbar_init(bar(L::kPFull + t), kBM / 32);  // one arrival per softmax warp
-      mbar_init(bar(L::kODone + t), 1);
+    for (int b = 0; b < L::kSBufs; ++b) {
+      mbar_init(bar(L::kSFull + b), 1);
+      mbar_init(bar(L::kPFull + b), kBM / 32);  // one arrival per softmax warp
     }
+    for (int t = 0; t < NQ; ++t) mbar_init(bar(L::kODone + t), 1);
     mbar_init(bar(L::kDrain), 1);
     fence_mbar_init();
   }
@@ -142,6 +146,23 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+  debug_context(tmem, args.err);
+  const Extent3 ext_q{D, N, args.BH}, ext_kv{D, Nk, args.BH / args.group};
+
+  // Ring items in the order the MMA warp consumes them.  Two sub-tiles: K_0, V_0,
+  // K_1, V_1, ...  One sub-tile (two score buffers): K_0, K_1, V_0, K_2, V_1, K_3,
+  // ..., V_{nb-1}, so S(j+2) is computed right after P(j) V_j.
+  auto ring_item = [&](int e, bool& is_v) -> int {
+    if constexpr (NQ != 1) {
+      is_v = e & 1;
+      return e >> 1;
+    } else {
+      if (e == 0) { is_v = false; return 0; }
+      if (e == 2 * nb - 1) { is_v = true; return nb - 1; }
+      is_v = !(e & 1);
+      return (e & 1) ? (e + 1) >> 1 : (e >> 1) - 1;
+    }
+  };
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
@@ -151,17 +172,25 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       for (int t = 0; t < NQ; ++t)
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sQ(t) + p * kPanelBytes, &tm_q, bar(L::kQFull), 64 * p, row0 + kBM * t, bh);
-      // K_0, V_0, K_1, V_1, ...: the order the MMA warp consumes them.
+          tma_load_box(sQ(t) + p * kPanelBytes, &tm_q, bar(L::kQFull), 64 * p, row0 + kBM * t, bh, ext_q, args.err);
+      int n = 0;  // ring loads issued
       for (int e = 0; e < 2 * nb; ++e) {
         const int s = e % STAGES, u = e / STAGES;
         if (u > 0 && !mbar_wait(bar(L::kEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
         mbar_expect_tx(bar(L::kFull + s), L::kTileBytes);
-        const CUtensorMap* m = (e & 1) ? &tm_v : &tm_k;
+        bool is_v;
+        const int blk = ring_item(e, is_v);
+        const CUtensorMap* m = is_v ? &tm_v : &tm_k;
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * (e >> 1), bh_kv);
+          tma_load_box(sRing(s) + p * kPanelBytes, m, bar(L::kFull + s), 64 * p, kBN * blk, bh_kv, ext_kv, args.err);
+        ++n;
       }
+      // Every copy this thread issued lands before the CTA exits, even when the
+      // consumers gave up after a timeout elsewhere (bounded waits, abort ignored).
+      mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < STAGES; ++s)
+        if (n > s) mbar_wait(bar(L::kFull + s), ((n - 1 - s) / STAGES) & 1, args.err, kErrTimeoutTma, false);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -169,31 +198,68 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       constexpr uint32_t kIdS = make_idesc_f16(BF16, kBM, kBN, false, false);
       constexpr uint32_t kIdPV = make_idesc_f16(BF16, kBM, D, false, true);
       constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // every operand here: 8-row groups 1024 B apart
-      auto issue_s = [&](int t, int s) {
+      // S of sub-tile t into score buffer `buf`, K from ring slot s
+      auto issue_s = [&](int t, int buf, int s) {
         const uint32_t a0 = sdesc_lo(sQ(t), 16), b0 = sdesc_lo(sRing(s), 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lohi(tmem + L::s_col(t), a0 + off, kHi, b0 + off, kHi, kIdS, kk > 0);
+          mma_ss_lohi(tmem + L::s_col(buf), a0 + off, kHi, b0 + off, kHi, kIdS, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int s, int j) {
+      // O_t += P V_j, P packed in score buffer `buf`, V from ring slot s
+      auto issue_pv = [&](int t, int buf, int s, int j) {
         const uint32_t b0 = sdesc_lo(sRing(s), kPanelBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)  // P_t: 8 TMEM columns (16 keys) per step
-          mma_ts_lohi(tmem + L::o_col(t), tmem + L::s_col(t) + 8 * kk, b0 + ((kk * 2048) >> 4), kHi, kIdPV,
+        for (int kk = 0; kk < kBN / 16; ++kk)  // P: 8 TMEM columns (16 keys) per step
+          mma_ts_lohi(tmem + L::o_col(t), tmem + L::s_col(buf) + 8 * kk, b0 + ((kk * 2048) >> 4), kHi, kIdPV,
                       (j > 0 || kk > 0) ? 1u : 0u);
       };
       auto wait_full = [&](int e) -> bool {
         return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
       };
       bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
+      if constexpr (NQ == 1) {
+        // S(0) S(1) | P(j) V_j, S(j+2) | ...: S(j+2) overwrites buffer j & 1 only after
+        // P(j) V_j has read it (one thread's MMAs execute in issue order).  Ring item
+        // of S(j): 0 for j = 0, else 2j - 1; of P(j) V_j: 2j + 2, or 2nb - 1 for the last.
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          mma_commit(bar(L::kSFull + 0));
+          mma_commit(bar(L::kEmpty + 0));
+          if (nb > 1 && (ok = wait_full(1))) {
+            tc_fence_after();
+            issue_s(0, 1, 1 % STAGES);
+            mma_commit(bar(L::kSFull + 1));
+            mma_commit(bar(L::kEmpty + 1 % STAGES));
+          }
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          const int b = j & 1;
+          const int ev = (j == nb - 1) ? 2 * nb - 1 : 2 * j + 2;
+          if (!(ok = mbar_wait(bar(L::kPFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax) && wait_full(ev)))
+            break;
+          tc_fence_after();
+          issue_pv(0, b, ev % STAGES, j);
+          mma_commit(bar(L::kODone + 0));
+          mma_commit(bar(L::kEmpty + ev % STAGES));
+          if (j + 2 < nb) {
+            const int ek = 2 * j + 3;
+            if (!(ok = wait_full(ek))) break;
+            tc_fence_after();
+            issue_s(0, b, ek % STAGES);
+            mma_commit(bar(L::kSFull + b));
+            mma_commit(bar(L::kEmpty + ek % STAGES));
+          }
+        }
+      } else {
       if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
           if (nblk[t] > 0) {
-            issue_s(t, 0);
+            issue_s(t, t, 0);
             mma_commit(bar(L::kSFull + t));
           }
         mma_commit(bar(L::kEmpty + 0));
@@ -210,17 +276,18 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
             ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, ev % STAGES, j);
+            issue_pv(t, t, ev % STAGES, j);
             mma_commit(bar(L::kODone + t));
           }
           if (t == NQ - 1) mma_commit(bar(L::kEmpty + ev % STAGES));  // last reader of V_j issued
           if (j + 1 < nblk[t]) {
-            issue_s(t, ek % STAGES);  // in order after P_t V_j, which read these columns
+            issue_s(t, t, ek % STAGES);  // in order after P_t V_j, which read these columns
             mma_commit(bar(L::kSFull + t));
           }
         }
         if (!ok) break;
         if (next) mma_commit(bar(L::kEmpty + ek % STAGES));
+      }
       }
       // Every MMA must have finished before TMEM can be released.
       mma_commit(bar(L::kDrain));
@@ -232,7 +299,6 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     const int r = ((warp & 3) << 5) + lane;  // row inside the sub-tile == TMEM lane
     const int q_row = row0 + kBM * t + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + L::s_col(t);
     const uint32_t tO = tmem + lane_base + L::o_col(t);
     const float c = args.scale_log2;
     const int key_limit = args.causal ? min(q_row + koff, Nk - 1) : Nk - 1;  // last key this row sees
@@ -241,7 +307,11 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     bool ok = true;
     const int my_blocks = nblk[t];
     for (int j = 0; j < my_blocks; ++j) {
-      ok = warp_wait(bar(L::kSFull + t), j & 1, args.err, kErrTimeoutMma);
+      // score buffer of this block and the parity of its barriers' phase
+      const int buf = NQ == 1 ? (j & 1) : t;
+      const uint32_t par = NQ == 1 ? ((j >> 1) & 1) : (j & 1);
+      const uint32_t tS = tmem + lane_base + L::s_col(buf);
+      ok = warp_wait(bar(L::kSFull + buf), par, args.err, kErrTimeoutMma);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -321,15 +391,22 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
         tmem_wait_st();
       }
       tc_fence_before();
-      warp_arrive(bar(L::kPFull + t));
+      warp_arrive(bar(L::kPFull + buf));
       m = m_use;
     }
     const bool has_rows = row0 + kBM * t < N;
     if (ok && has_rows) {
       // A sub-tile whose rows see no key at all writes O = 0 and L = -inf; it still
       // waits for its Q tile to land before reusing that shared memory.
-      ok = my_blocks > 0 ? warp_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma)
-                         : warp_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
+      // With two score buffers (NQ = 1) up to two P V products can still be in flight
+      // here, so the parity of ODone would be ambiguous: wait for the one-phase
+      // drain barrier the MMA warp commits after its last product instead.
+      if (my_blocks == 0)
+        ok = warp_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma);
+      else if constexpr (NQ == 1)
+        ok = warp_wait(bar(L::kDrain), 0, args.err, kErrTimeoutMma);
+      else
+        ok = warp_wait(bar(L::kODone + t), (my_blocks - 1) & 1, args.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -366,7 +443,8 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     named_bar_sync(1 + t, kBM);
     if (ok && has_rows && r == 0) {
 #pragma unroll
-      for (int p = 0; p < L::kPanels; ++p) tma_store_3d(&tm_o, sQ(t) + p * kPanelBytes, 64 * p, row0 + kBM * t, bh);
+      for (int p = 0; p < L::kPanels; ++p)
+        tma_store_box(&tm_o, sQ(t) + p * kPanelBytes, 64 * p, row0 + kBM * t, bh, ext_q, args.err);
       tma_store_commit();
       tma_store_wait0();
     }
@@ -374,6 +452,23 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kDebug) {
+    // every barrier completed as many phases as the protocol says
+    if (threadIdx.x == 0 && no_abort(args.err)) {
+      check_phase(bar(L::kQFull), 1, args.err, L::kQFull);
+      for (int s = 0; s < STAGES; ++s) {
+        check_phase(bar(L::kFull + s), count_mod(2 * nb, s, STAGES), args.err, L::kFull + s);
+        check_phase(bar(L::kEmpty + s), count_mod(2 * nb, s, STAGES), args.err, L::kEmpty + s);
+      }
+      for (int b = 0; b < L::kSBufs; ++b) {
+        const uint32_t n_s = NQ == 1 ? count_mod(nb, b, 2) : (uint32_t)nblk[b];
+        check_phase(bar(L::kSFull + b), n_s, args.err, L::kSFull + b);
+        check_phase(bar(L::kPFull + b), n_s, args.err, L::kPFull + b);
+      }
+      for (int t = 0; t < NQ; ++t) check_phase(bar(L::kODone + t), nblk[t], args.err, L::kODone + t);
+      check_phase(bar(L::kDrain), 1, args.err, L::kDrain);
+    }
+  }
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);

@@ -99,6 +99,11 @@ cudaError_t launch_bwd_main_256(bool bf16, const CUtensorMap& q, const CUtensorM
 // Failure-detection self-test: one bounded wait that nothing completes.
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 
+#ifdef FA_DEBUG
+// FA_DEBUG builds: one device-side check of the given kind handed a value that breaks it.
+cudaError_t launch_selftest_check(uint32_t* err, int kind, cudaStream_t stream);
+#endif
+
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream);
 

@@ -20,8 +20,28 @@ enum : uint32_t {
   kErrTimeoutRing = 1u << 3,      // the producer never got a free ring slot
   kErrTimeoutSync = 1u << 4,      // a warpgroup barrier never completed
   kErrSelfTest = 1u << 5,         // the failure-detection self-test's wait (expected to give up)
+  kErrDebugCheck = 1u << 6,       // FA_DEBUG builds: a bounds, alignment or phase check failed
   kErrAborted = 1u << 31,         // set with the first failure: every later wait gives up at once
 };
+
+// What a failed FA_DEBUG check was about (err[1] = kDbgBase | kind when it is the
+// first failure; err[3] then holds the offending value).
+enum : uint32_t {
+  kDbgBase = 0x100u,
+  kDbgTmaCol = 1,      // TMA box column not a multiple of 64 or outside the head dimension
+  kDbgTmaRow = 2,      // TMA box row outside [0, rows rounded up to 128)
+  kDbgTmaPlane = 3,    // TMA box plane outside [0, planes)
+  kDbgTmemCol = 4,     // TMEM access past the 512 allocated columns
+  kDbgTmemLane = 5,    // TMEM lane quarter outside the 128 lanes
+  kDbgBulk = 6,        // bulk copy source outside its row vector
+  kDbgPhase = 7,       // an mbarrier ended the CTA with a phase count of the wrong parity
+};
+
+#ifdef FA_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
 
 // Device error record: [0] the bits above; [1] the code of the first failure;
 // [2] its CTA index; [3] its barrier's shared-memory offset.
@@ -92,6 +112,26 @@ static __device__ __noinline__ void record_timeout(uint32_t* err, uint32_t code,
   }
   atomicOr(err, code | kErrAborted);
 }
+
+// Records a failed FA_DEBUG check: the first failure's code, CTA and value, and
+// the check bit.  It does not set the abort bit: the caller clamps the access to
+// a safe value and the kernel runs on, so one launch reports every kind of slip.
+static __device__ __noinline__ void record_check(uint32_t* err, uint32_t kind, uint32_t value) {
+  if (!err) return;
+  if (atomicCAS(err + 1, 0u, kDbgBase | kind) == 0u) {
+    err[2] = blockIdx.x;
+    err[3] = value;
+  }
+  atomicOr(err, kErrDebugCheck);
+}
+
+#ifdef FA_DEBUG
+// Per-CTA context of the TMEM checks (debug builds only): the allocation's base
+// address and the error record.  Each kernel sets them once, right after its
+// TMEM allocation (debug_context).
+static __shared__ uint32_t dbg_tmem_base;
+static __shared__ uint32_t* dbg_err_ptr;
+#endif
 
 // The final drain of a CTA's tensor-core work passes honor_abort = false: it
 // always waits (bounded) for the MMAs already issued before TMEM is released.
@@ -186,6 +226,37 @@ __device__ __forceinline__ void tma_store_wait_read0() {
 __device__ __forceinline__ void tma_store_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05: TMEM
+// FA_DEBUG builds: a TMEM address (lane quarter in bits 16-31, column in 0-15) and
+// the columns an access spans, against the CTA's 512 allocated columns and 128
+// lanes; a failure is recorded and the access goes to the allocation's base.
+// Identity otherwise.
+__device__ __forceinline__ uint32_t tm(uint32_t taddr, uint32_t ncols) {
+#ifdef FA_DEBUG
+  const uint32_t base = dbg_tmem_base;
+  const uint32_t col = (taddr & 0xFFFFu) - (base & 0xFFFFu), lane = (taddr >> 16) - (base >> 16);
+  if (col + ncols > 512u) {
+    record_check(dbg_err_ptr, kDbgTmemCol, col);
+    return base;
+  }
+  if (lane >= 128u || (lane & 31u)) {
+    record_check(dbg_err_ptr, kDbgTmemLane, lane);
+    return base;
+  }
+#endif
+  return taddr;
+}
+// Sets the TMEM check context; every thread of the CTA calls it after reading the
+// allocation's base (it synchronizes the CTA in FA_DEBUG builds, nothing otherwise).
+__device__ __forceinline__ void debug_context(uint32_t tmem_base, uint32_t* err) {
+#ifdef FA_DEBUG
+  if (threadIdx.x == 0) {
+    dbg_tmem_base = tmem_base;
+    dbg_err_ptr = err;
+  }
+  __syncthreads();
+#endif
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");
@@ -202,21 +273,21 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-               : "r"(taddr));
+               : "r"(tm(taddr, 32)));
 }
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               :: "r"(tm(taddr, 32)), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
 }
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+               :: "r"(tm(taddr, 16)), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
                   "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                : "memory");
 }
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tm(taddr, 4)), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
 }
@@ -229,12 +300,14 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
 }
 
 // ---------------------------------------------------------------- tcgen05: MMA
+// Accumulator columns an MMA writes: N, from bits 17-22 of the instruction descriptor.
+__device__ __forceinline__ uint32_t idesc_n(uint32_t idesc) { return ((idesc >> 17) & 0x3Fu) << 3; }
 // D[tmem] (+)= A[smem] * B[smem], kind::f16 (fp16 or bf16 inputs, fp32 accumulate).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tm(d_tmem, idesc_n(idesc))),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -244,8 +317,8 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                                        uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tm(d_tmem, idesc_n(idesc))),
+      "r"(tm(a_tmem, 8)), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // The same MMAs with the shared-memory descriptors passed as (low, high) 32-bit
@@ -257,7 +330,7 @@ __device__ __forceinline__ void mma_ss_lohi(uint32_t d_tmem, uint32_t a_lo, uint
   asm volatile(
       "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %6, 0;\n"
       " mov.b64 a, {%1, %2};\n mov.b64 b, {%3, %4};\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n}\n" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n}\n" ::"r"(tm(d_tmem, idesc_n(idesc))),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -265,8 +338,8 @@ __device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, ui
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n .reg .b64 b;\n setp.ne.b32 p, %5, 0;\n mov.b64 b, {%2, %3};\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n}\n" ::"r"(tm(d_tmem, idesc_n(idesc))),
+      "r"(tm(a_tmem, 8)), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Low and high halves of the 128-byte-swizzle descriptor (see make_sdesc_sw128).
@@ -383,6 +456,79 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
 // 8-row group, the layout TMA writes with 128-byte swizzling.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
   return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------- FA_DEBUG checks
+// Extents of a [planes, rows, cols] tensor as a TMA descriptor sees it.
+struct Extent3 {
+  int cols, rows, planes;
+};
+// In FA_DEBUG builds: checks a box origin against the tensor (column a multiple of
+// 64 -- 128 bytes, so the 16-byte rule holds -- and inside the head dimension; row
+// inside the rows rounded up to 256, the furthest any tile of these kernels
+// starts: the forward's second 128-row sub-tile of a 256-row block; plane inside
+// the planes), records a failure and clamps the origin to a valid one.  Compiles
+// to nothing otherwise.
+__device__ __forceinline__ void check_box(int& c0, int& c1, int& c2, const Extent3& e, uint32_t* err) {
+  if constexpr (kDebug) {
+    if (c0 < 0 || (c0 & 63) || c0 >= e.cols) { record_check(err, kDbgTmaCol, (uint32_t)c0); c0 = 0; }
+    if (c1 < 0 || c1 >= (e.rows + 255) / 256 * 256) { record_check(err, kDbgTmaRow, (uint32_t)c1); c1 = 0; }
+    if (c2 < 0 || c2 >= e.planes) { record_check(err, kDbgTmaPlane, (uint32_t)c2); c2 = 0; }
+  }
+}
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2,
+                                             const Extent3& e, uint32_t* err) {
+  check_box(c0, c1, c2, e, err);
+  tma_load_3d(dst, m, bar, c0, c1, c2);
+}
+__device__ __forceinline__ void tma_store_box(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2,
+                                              const Extent3& e, uint32_t* err) {
+  check_box(c0, c1, c2, e, err);
+  tma_store_3d(m, src, c0, c1, c2);
+}
+// In FA_DEBUG builds: a bulk copy of `bytes` from element `first` of a row vector
+// of `count` floats must stay inside the vector and start 16-byte aligned; a
+// failure is recorded and the copy starts at element 0 instead.
+__device__ __forceinline__ void check_rows(long long& first, uint32_t bytes, long long count, uint32_t* err) {
+  if constexpr (kDebug) {
+    if (first < 0 || first + bytes / 4 > count || (first & 3)) {
+      record_check(err, kDbgBulk, (uint32_t)first);
+      first = 0;
+    }
+  }
+}
+__device__ __forceinline__ void bulk_load_rows(uint32_t dst, const float* vec, long long first, uint32_t bytes,
+                                               long long count, uint32_t bar, uint32_t* err) {
+  check_rows(first, bytes, count, err);
+  bulk_load(dst, vec + first, bytes, bar);
+}
+// At CTA exit (all threads past the final barrier): an mbarrier that completed
+// `phases` phases has current phase parity phases & 1.  A wrong count of
+// arrivals or commits anywhere in the CTA's protocol shows up here.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+// Indices i in [0, n) with i % m == s: the phases a barrier of stage s completes
+// when n items go round a ring of m stages.
+__device__ __forceinline__ uint32_t count_mod(int n, int s, int m) { return n > s ? (uint32_t)((n - 1 - s) / m + 1) : 0u; }
+// True when no wait of the grid has given up (phase counts are only meaningful then).
+__device__ __forceinline__ bool no_abort(const uint32_t* err) {
+  return !(*reinterpret_cast<const volatile uint32_t*>(err) & kErrAborted);
+}
+__device__ __forceinline__ void check_phase(uint32_t bar, uint32_t phases, uint32_t* err, uint32_t id) {
+  if constexpr (kDebug) {
+    // test_wait.parity(p) is true once the phase with parity p has completed, i.e.
+    // while the current phase's parity differs from p
+    if (mbar_test_wait(bar, phases & 1u)) record_check(err, kDbgPhase, (id << 16) | (phases & 0xFFFFu));
+  }
 }
 
 }  // namespace fa

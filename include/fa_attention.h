@@ -55,7 +55,8 @@ typedef enum {
   FA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,      /* backward workspace missing or smaller than fa_bwd_workspace_size */
   FA_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
-  FA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up on a bounded wait (see fa_check_device_status) */
+  FA_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up on a bounded wait (see fa_check_device_status) */
+  FA_ERR_DEVICE_CHECK = 7    /* debug builds: a device-side bounds, alignment or phase check failed */
 } fa_status;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -174,10 +175,40 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 
 /*
  * Synchronizes `stream`, then reads and clears the device error word of the
- * current device.  FA_OK if no kernel gave up on a wait since the last check,
- * FA_ERR_DEVICE_TIMEOUT otherwise, FA_ERR_CUDA if the synchronization failed.
+ * current device.  FA_OK if no kernel gave up on a wait (and, in a debug build,
+ * no device-side check failed) since the last check; otherwise the kind of the
+ * first failure: FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_CHECK.  FA_ERR_CUDA if
+ * the synchronization failed.
  */
 fa_status fa_check_device_status(fa_stream_t stream);
+
+/*
+ * Debug builds (the library compiled with -DFA_DEBUG, `build(debug=True)` of the
+ * Python build script: libfa_attention_debug.so) check on the device, before
+ * every TMA copy, tensor-memory access and tensor-core product and at every
+ * CTA's exit:
+ *   - the box origin of each TMA copy: column a multiple of 64 inside the head
+ *     dimension, row inside the tensor's rows rounded up to 256, plane inside
+ *     the tensor's planes (kinds 1, 2, 3);
+ *   - each tensor-memory address and the columns its access spans against the
+ *     CTA's 512 allocated columns and 128 lanes (kinds 4, 5);
+ *   - each bulk copy of L log2 e and D rows against the workspace's rows (kind 6);
+ *   - at CTA exit, that every mbarrier completed the number of phases the
+ *     kernel's protocol says (kind 7; only when no wait gave up).
+ * A failed check records the error bit 64, the code 0x100 | kind, the CTA and
+ * the offending value in the device error record, clamps the access to a safe
+ * one and lets the kernel run on (it never traps); fa_check_device_status then
+ * returns FA_ERR_DEVICE_CHECK and fa_last_device_error_detail gives the record.
+ * This is the stand-in for a memory checker where none can be run.
+ *
+ * fa_selftest_device_check(kind, stream) makes check `kind` (1..7) fail once on
+ * purpose: one thread hands the check a value that breaks its rule and discards
+ * the clamped result, so nothing is copied or accessed.  Returns FA_OK
+ * (asynchronous on `stream`), FA_ERR_INVALID_ARG for another kind,
+ * FA_ERR_UNSUPPORTED in a release build (the checks are compiled out) or on a
+ * device other than sm_103, FA_ERR_CUDA if the launch failed.
+ */
+fa_status fa_selftest_device_check(int kind, fa_stream_t stream);
 
 /*
  * Host-buffer entry points (a runtime convenience; the attention method has no
@@ -259,9 +290,10 @@ uint32_t fa_last_device_error_bits(void);
 /*
  * The error record behind it: out4[0] the bits, out4[1] the code of the first
  * wait that gave up (1 TMA tile, 2 tensor-core commit, 4 elementwise output,
- * 8 ring slot, 16 warpgroup barrier, 32 self-test), out4[2] that CTA's index,
+ * 8 ring slot, 16 warpgroup barrier, 32 self-test; 0x100 | kind for a failed
+ * debug-build check), out4[2] that CTA's index,
  * out4[3] its
- * barrier's shared-memory address.  After the first failure every other wait
+ * barrier's shared-memory address (for a check: the offending value).  After the first failure every other wait
  * of the grid gives up at once (bit 31), and kernels launched before the next
  * fa_check_device_status stop early: their results are not valid.
  */

@@ -39,6 +39,11 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in _lib.SIGNATURES, f"binding lacks {name}"
 
 
+def test_device_check_selftest_needs_the_checked_build(lib):
+    # the release library has the device-side checks compiled out
+    assert lib.fa_selftest_device_check(1, None) == 2
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS.items():
         assert lib.fa_status_string(code).decode() == name
