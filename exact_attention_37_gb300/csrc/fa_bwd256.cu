@@ -501,21 +501,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // CTA -> (role, block, head).  First the key-block CTAs, the dK and dV CTAs of one
-  // (key/value head, key block) side by side, lowest key blocks first (under the
-  // causal mask they see the most query blocks); then the dQ CTAs, the last query
-  // blocks first.  Heads in groups (grouped_tile) so the running CTAs' tiles stay in L2.
+  // CTA -> (role, block, head), by groups of G key/value heads (args.head_group_kv):
+  // a group's dK and dV CTAs (the pair of one key block side by side, lowest key
+  // blocks first: under the causal mask they see the most query blocks), then the
+  // dQ CTAs of its G * group query heads (the last query blocks first).  The query
+  // heads of key/value heads [a, a + G) are [a * group, (a + G) * group), so a
+  // group's dQ CTAs read the same K, V, Q, dO its key-block CTAs have just brought
+  // into L2, and the light CTAs that end one group run beside the heavy ones that
+  // start the next.
   const int nkb = (args.Nk + kRes - 1) / kRes;
   const int nqb = (args.N + kRes - 1) / kRes;
-  const unsigned n_kv = 2u * (unsigned)nkb * (unsigned)args.BHkv;
+  const int grp = args.group;
+  const int G = max(1, min(args.head_group_kv, args.BHkv));
+  const unsigned per_full = (unsigned)G * (2u * (unsigned)nkb + (unsigned)nqb * (unsigned)grp);
+  const int g = (int)(blockIdx.x / per_full);
+  const int h0 = g * G;                        // first key/value head of the group
+  const int Gg = min(G, args.BHkv - h0);       // heads in this group (the last may be short)
+  unsigned t = blockIdx.x - (unsigned)g * per_full;
+  const unsigned n_kv = 2u * (unsigned)nkb * (unsigned)Gg;
   int role, blk, head;
-  if (blockIdx.x < n_kv) {
-    role = (blockIdx.x & 1) ? kRoleDV : kRoleDK;
-    grouped_tile(blockIdx.x >> 1, args.BHkv, nkb, args.head_group_kv, blk, head);
+  if (t < n_kv) {
+    role = (t & 1) ? kRoleDV : kRoleDK;
+    t >>= 1;
+    blk = (int)(t / (unsigned)Gg);
+    head = h0 + (int)(t % (unsigned)Gg);
   } else {
+    t -= n_kv;
+    const unsigned nq_heads = (unsigned)Gg * (unsigned)grp;
     role = kRoleDQ;
-    grouped_tile(blockIdx.x - n_kv, args.BH, nqb, args.head_group_q, blk, head);
-    blk = nqb - 1 - blk;
+    blk = nqb - 1 - (int)(t / nq_heads);
+    head = h0 * grp + (int)(t % nq_heads);
   }
 
   if (threadIdx.x == 0) {
