@@ -40,19 +40,35 @@ def _inputs():
     return files
 
 
-def up_to_date(lib: str = LIB) -> bool:
+def _flags_file(objdir: str) -> str:
+    return os.path.join(objdir, "flags.txt")
+
+
+def up_to_date(lib: str = LIB, objdir: str = OBJDIR, flags=()) -> bool:
+    """The library exists, is newer than every source, and was built with `flags`."""
     if not os.path.exists(lib):
+        return False
+    try:
+        with open(_flags_file(objdir)) as f:
+            if f.read() != " ".join(flags):
+                return False
+    except OSError:
         return False
     t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: bool = False,
+          nvtx: bool | None = None) -> str:
     """Compile and link the library if needed; returns its path.  ``debug`` builds
-    the checked variant (``libfa_attention_debug.so``) instead."""
+    the checked variant (``libfa_attention_debug.so``) instead; ``nvtx`` (default:
+    the FA_NVTX environment variable is set to 1) marks every C-ABI call with an
+    NVTX range."""
     lib, objdir = (LIB_DEBUG, OBJDIR_DEBUG) if debug else (LIB, OBJDIR)
-    extra_flags = (*extra_flags, "-DFA_DEBUG") if debug else tuple(extra_flags)
-    if not force and up_to_date(lib):
+    if nvtx is None:
+        nvtx = os.environ.get("FA_NVTX") == "1"
+    extra_flags = (*extra_flags, *(["-DFA_DEBUG"] if debug else []), *(["-DFA_NVTX"] if nvtx else []))
+    if not force and up_to_date(lib, objdir, extra_flags):
         return lib
     os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
@@ -81,6 +97,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: boo
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
     os.replace(tmp, lib)
+    with open(_flags_file(objdir), "w") as f:
+        f.write(" ".join(extra_flags))
     return lib
 
 

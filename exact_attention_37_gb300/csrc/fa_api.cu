@@ -14,6 +14,7 @@
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
+#include "fa_nvtx.h"
 #include "ptx.cuh"
 
 namespace fa {
@@ -192,6 +193,7 @@ extern "C" {
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
                     int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  const fa::NvtxRange range("fa_fwd_ex");
   fa_status st = check_common(B, H, H_kv, N_q, N_k, d, scale, (int)dtype);
   if (st != FA_OK) return st;
   if ((long long)B * H * N_q == 0) return FA_OK;  // empty problem
@@ -237,6 +239,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
                     int N_q, int N_k, int d, float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  const fa::NvtxRange range("fa_bwd_ex");
   fa_status st = check_common(B, H, H_kv, N_q, N_k, d, scale, (int)dtype);
   if (st != FA_OK) return st;
   if ((long long)B * H * N_q == 0) {
@@ -333,6 +336,7 @@ extern "C" {
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, fa_dtype dtype, fa_stream_t stream) {
+  const fa::NvtxRange range("fa_bwd_noalloc");
   fa_status st = check_common(B, H, H, N, N, d, scale, (int)dtype);
   if (st != FA_OK) return st;
   if ((long long)B * H * N == 0) return FA_OK;

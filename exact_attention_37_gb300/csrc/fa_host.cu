@@ -14,6 +14,7 @@
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
+#include "fa_nvtx.h"
 
 namespace fa {
 namespace {
@@ -247,6 +248,7 @@ size_t fa_host_scratch_size(int B, int H, int N, int d, int with_backward) {
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dev_scratch,
                       size_t scratch_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
                       int chunks, fa_stream_t stream) {
+  const fa::NvtxRange range("fa_fwd_host");
   return run_host(q, k, v, nullptr, o, lse, nullptr, nullptr, nullptr, dev_scratch, scratch_bytes, B, H, N, d,
                   scale, causal, dtype, chunks, stream, false);
 }
@@ -254,6 +256,7 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
 fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
                           void* dq, void* dk, void* dv, void* dev_scratch, size_t scratch_bytes, int B, int H, int N,
                           int d, float scale, int causal, fa_dtype dtype, int chunks, fa_stream_t stream) {
+  const fa::NvtxRange range("fa_fwd_bwd_host");
   return run_host(q, k, v, dout, o, lse, dq, dk, dv, dev_scratch, scratch_bytes, B, H, N, d, scale, causal, dtype,
                   chunks, stream, true);
 }

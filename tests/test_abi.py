@@ -214,3 +214,14 @@ def test_cta_head_group_at_the_workload_shapes(lib):
     assert _lib.fa_cta_head_group(32, 256, 32 << 20, True, 152) == 2  # 32k context, backward
     assert _lib.fa_cta_head_group(64, 16, 1 << 20, False, 152) == 64  # small heads: one group
     assert lib.fa_cta_head_group(0, 4, 1, 0, 152) == -1
+
+
+def test_nvtx_ranges_compile(tmp_path):
+    """The optional NVTX build (-DFA_NVTX: a range around every C-ABI call) compiles."""
+    import subprocess
+
+    for src in ("fa_api.cu", "fa_host.cu"):
+        cmd = [fabuild.nvcc(), *fabuild.ARCH, *fabuild.FLAGS, "-DFA_NVTX", "-c", os.path.join(fabuild.CSRC, src),
+               "-o", str(tmp_path / (src + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
