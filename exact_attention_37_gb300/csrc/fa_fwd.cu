@@ -54,6 +54,10 @@ struct FwdLayout {
   // One sub-tile (NQ = 1) keeps two score buffers, used by alternate key blocks, so
   // the scores of block j+1 are computed while the softmax works on block j.
   static constexpr int kSBufs = NQ == 1 ? 2 : NQ;
+  // Two sub-tiles at d = 64 leave 128 TMEM columns free: each sub-tile's P goes to
+  // its own 64 columns there instead of into its S columns, so S(j+1) may overwrite
+  // S(j) as soon as the softmax has read it, not only after P(j) V has run.
+  static constexpr bool kSepP = NQ == 2 && D == 64;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kFull = 1;
@@ -62,7 +66,8 @@ struct FwdLayout {
   static constexpr int kPFull = kSFull + kSBufs;  // one per score buffer
   static constexpr int kODone = kPFull + kSBufs;  // one per sub-tile
   static constexpr int kDrain = kODone + NQ;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSFree = kDrain + 1;        // kSepP: one per sub-tile, S read out
+  static constexpr int kNumBars = kSFree + (kSepP ? NQ : 0);
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024 B
@@ -71,7 +76,9 @@ struct FwdLayout {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t s_col(int b) { return 128u * b; }
   static constexpr uint32_t o_col(int t) { return 128u * kSBufs + (uint32_t)D * t; }
-  static_assert(128 * kSBufs + D * NQ <= 512, "TMEM budget");
+  // where P of sub-tile t is packed: its S columns, or (kSepP) 64 columns after O
+  static constexpr uint32_t p_col(int t) { return kSepP ? 128u * kSBufs + (uint32_t)D * NQ + 64u * t : s_col(t); }
+  static_assert(128 * kSBufs + D * NQ + (kSepP ? 64 * NQ : 0) <= 512, "TMEM budget");
   static_assert(kBytes + 1024 <= 232448, "shared memory budget");
 };
 
@@ -129,6 +136,8 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       mbar_init(bar(L::kPFull + b), kBM / 32);  // one arrival per softmax warp
     }
     for (int t = 0; t < NQ; ++t) mbar_init(bar(L::kODone + t), 1);
+    if constexpr (L::kSepP)
+      for (int t = 0; t < NQ; ++t) mbar_init(bar(L::kSFree + t), kBM / 32);
     mbar_init(bar(L::kDrain), 1);
     fence_mbar_init();
   }
@@ -150,10 +159,11 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
   const Extent3 ext_q{D, N, args.BH}, ext_kv{D, Nk, args.BH / args.group};
 
   // Ring items in the order the MMA warp consumes them.  Two sub-tiles: K_0, V_0,
-  // K_1, V_1, ...  One sub-tile (two score buffers): K_0, K_1, V_0, K_2, V_1, K_3,
-  // ..., V_{nb-1}, so S(j+2) is computed right after P(j) V_j.
+  // K_1, V_1, ...  One sub-tile (two score buffers), or two with separate P buffers:
+  // K_0, K_1, V_0, K_2, V_1, K_3, ..., V_{nb-1}, the next block's K before this
+  // block's V.
   auto ring_item = [&](int e, bool& is_v) -> int {
-    if constexpr (NQ != 1) {
+    if constexpr (NQ != 1 && !L::kSepP) {
       is_v = e & 1;
       return e >> 1;
     } else {
@@ -212,14 +222,52 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
         const uint32_t b0 = sdesc_lo(sRing(s), kPanelBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)  // P: 8 TMEM columns (16 keys) per step
-          mma_ts_lohi(tmem + L::o_col(t), tmem + L::s_col(buf) + 8 * kk, b0 + ((kk * 2048) >> 4), kHi, kIdPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_lohi(tmem + L::o_col(t), tmem + (L::kSepP ? L::p_col(t) : L::s_col(buf)) + 8 * kk,
+                      b0 + ((kk * 2048) >> 4), kHi, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
       auto wait_full = [&](int e) -> bool {
         return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
       };
       bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
-      if constexpr (NQ == 1) {
+      if constexpr (L::kSepP) {
+        // S_0(0) S_1(0) | S_t(j+1) once the softmax has read S_t(j), then P_t(j) V_j |
+        // ...  Ring item of K(j+1): 2j + 1; of V_j: 2j + 2, or 2nb - 1 for the last.
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < NQ; ++t)
+            if (nblk[t] > 0) {
+              issue_s(t, t, 0);
+              mma_commit(bar(L::kSFull + t));
+            }
+          mma_commit(bar(L::kEmpty + 0));
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          if (j + 1 < nb) {
+            const int ek = 2 * j + 1;
+            if (!(ok = wait_full(ek))) break;
+            for (int t = 0; t < NQ; ++t)
+              if (j + 1 < nblk[t]) {
+                if (!(ok = mbar_wait(bar(L::kSFree + t), j & 1, args.err, kErrTimeoutSoftmax))) break;
+                tc_fence_after();
+                issue_s(t, t, ek % STAGES);
+                mma_commit(bar(L::kSFull + t));
+              }
+            if (!ok) break;
+            mma_commit(bar(L::kEmpty + ek % STAGES));
+          }
+          const int ev = (j == nb - 1) ? 2 * nb - 1 : 2 * j + 2;
+          if (!(ok = wait_full(ev))) break;
+          for (int t = 0; t < NQ; ++t)
+            if (j < nblk[t]) {
+              if (!(ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax))) break;
+              tc_fence_after();
+              issue_pv(t, t, ev % STAGES, j);
+              mma_commit(bar(L::kODone + t));
+            }
+          if (!ok) break;
+          mma_commit(bar(L::kEmpty + ev % STAGES));
+        }
+      } else if constexpr (NQ == 1) {
         // S(0) S(1) | P(j) V_j, S(j+2) | ...: S(j+2) overwrites buffer j & 1 only after
         // P(j) V_j has read it (one thread's MMAs execute in issue order).  Ring item
         // of S(j): 0 for j = 0, else 2j - 1; of P(j) V_j: 2j + 2, or 2nb - 1 for the last.
@@ -320,6 +368,10 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int h = 0; h < 4; ++h) reg_fence32(sr[h]);
+      if constexpr (L::kSepP) {
+        tc_fence_before();
+        warp_arrive(bar(L::kSFree + t));  // S_t may be overwritten by the next block's scores
+      }
 
       float s[128];
 #pragma unroll
@@ -351,6 +403,19 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       // d = 64 stores a quarter row at a time (fewer live registers; faster there),
       // d = 128 half a row.
       constexpr int kPE = D == 64 ? 32 : 64;  // elements of P per store
+      // With separate P buffers, P(j) overwrites P(j-1): wait until P(j-1) V has run.
+      // (S(j) was issued after P(j-2) V, so that phase has completed: the parity is
+      // unambiguous.)
+      bool o_done = false;
+      if constexpr (L::kSepP) {
+        if (j > 0) {
+          ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          o_done = true;
+        }
+      }
+      const uint32_t tP = L::kSepP ? tmem + lane_base + L::p_col(t) : tS;
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
       for (int h = 0; h < 128 / kPE; ++h) {
@@ -367,17 +432,19 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
           pw[((i % kPE) >> 1) + 1] = pack2<BF16>(p2, p3);
         }
         if constexpr (kPE == 64)
-          tmem_st_32x32b_x32(tS + 32 * h, pw);
+          tmem_st_32x32b_x32(tP + 32 * h, pw);
         else
-          tmem_st_32x32b_x16(tS + 16 * h, pw);
+          tmem_st_32x32b_x16(tP + 16 * h, pw);
       }
       l = l * alpha + ((l0 + l1) + (l2 + l3));
       tmem_wait_st();
       // O_t is rescaled only when the reference moved, after the previous P V is done.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
+        if (!o_done) {
+          ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
@@ -467,6 +534,8 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       }
       for (int t = 0; t < NQ; ++t) check_phase(bar(L::kODone + t), nblk[t], args.err, L::kODone + t);
       check_phase(bar(L::kDrain), 1, args.err, L::kDrain);
+      if constexpr (L::kSepP)
+        for (int t = 0; t < NQ; ++t) check_phase(bar(L::kSFree + t), nblk[t], args.err, L::kSFree + t);
     }
   }
   if (warp == kWarpMma) {
