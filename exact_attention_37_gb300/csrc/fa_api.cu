@@ -45,6 +45,48 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The current CUDA context (driver API, looked up through the runtime's entry-point
+// query so the library needs no link against libcuda), or nullptr.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// Device address of a __device__ symbol on the current device, cached per device
+// and keyed on the device's current context: after cudaDeviceReset (a new primary
+// context) the address is looked up again instead of reusing a stale one.
+struct SymbolCache {
+  std::mutex mu;
+  CUcontext ctx[kMaxDevices] = {};
+  void* ptr[kMaxDevices] = {};
+  void* get(const void* symbol) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    // (before the first runtime call on a thread no context may be current yet: the
+    // lookup below makes it current, and the next call re-keys the cache once)
+    const CUcontext c = current_context();
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev] || c != ctx[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+      ptr[dev] = p;
+      ctx[dev] = c;
+    }
+    return ptr[dev];
+  }
+};
+
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -52,19 +94,10 @@ int sm_count() {
   return sms > 0 ? sms : 1;
 }
 
-// Address of the error word on the current device (looked up once per device).
+// Address of the error word on the current device.
 uint32_t* error_word_ptr() {
-  static uint32_t* ptrs[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<uint32_t*>(p);
-  }
-  return ptrs[dev];
+  static SymbolCache cache;
+  return static_cast<uint32_t*>(cache.get(g_error_word));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -314,19 +347,10 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch on the current device.
 void* noalloc_scratch_ptr() {
-  static void* ptrs[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
-  }
-  return ptrs[dev];
+  static SymbolCache cache;
+  return cache.get(g_noalloc_scratch);
 }
 }  // namespace
 }  // namespace fa

@@ -157,12 +157,11 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * of 128 (with B*H = 1, N up to 4,194,304 rows).
  *
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it for the process; make that first call
- * before any stream capture.  cudaDeviceReset (or anything else that destroys
- * the device's primary context) invalidates the cached address, as it does the
- * library's device error record: do not call the library on that device again
- * in the same process.  No call allocates: no cudaMalloc, cudaFree or
- * allocating library routine.  Every call overwrites the whole scratch region
+ * that device current) and caches it, keyed on the device's current CUDA
+ * context; make that first call before any stream capture.  After
+ * cudaDeviceReset (a new primary context) the next call looks the address up
+ * again, as it does the library's device error record.  No call allocates: no
+ * cudaMalloc, cudaFree or allocating library routine.  Every call overwrites the whole scratch region
  * it uses before reading it (the D pre-pass writes every row vector, padding
  * rows included), so stale contents from an earlier call never leak into a
  * result.  All calls share the one array: two calls whose kernels overlap on
