@@ -19,8 +19,10 @@
 //           into tensor memory and is the A operand of S^T = K Q^T; V stays in
 //           shared memory for dP^T = V dO^T; Q and dO stream in 64-row tiles;
 //           dK += dS^T Q with dS^T packed in tensor memory.
-//   dV CTA  (same block): K in tensor memory, S^T = K Q^T into two alternating
-//           64-column buffers, P^T packed in place, dV += P^T dO.
+//   dV CTA  (same block): only S^T = K Q^T and dV += P^T dO, so it streams
+//           128-row Q and dO tiles (N = 128 score products) with K in shared
+//           memory, and keeps P^T apart from S^T in tensor memory so the next
+//           block's scores run while the elementwise warps exponentiate.
 //   dQ CTA  (query head, 128-row query block): queries on TMEM lanes.  Q in tensor
 //           memory is the A operand of S = Q K^T; dO stays in shared memory for
 //           dP = dO V^T; K and V stream in 64-key tiles; dQ += dS K.
@@ -33,13 +35,13 @@
 // in tensor memory.  The dK and dV CTAs of one key block are adjacent in the
 // grid (they stream the same Q and dO tiles), and the dQ CTAs follow them.
 //
-// Tensor memory: columns 0-127 hold the resident operand (K or Q, 16-bit pairs),
-// 128-191 and 192-255 two 64-column score buffers (S and dP, or two S^T), 256-511
-// the gradient accumulator.  Shared memory: the stationary 128-row tile (64 KB),
-// three 64-row stages of the operand read by the score and gradient products,
-// two of the operand read by the second product (32 KB each), and the L, D
-// values of each query stage.  Warps: 0-7 elementwise (two warpgroups, 32 tile
-// columns each), 8 TMA, 9 MMA.
+// dK and dQ CTAs: tensor memory columns 0-127 hold the resident operand (K or Q,
+// 16-bit pairs), 128-191 and 192-255 the S and dP buffers, 256-511 the gradient
+// accumulator; shared memory holds the stationary 128-row tile (64 KB), three
+// 64-row stages of the operand read by the score and gradient products, two of
+// the operand read by the second product (32 KB each), and the L, D values of
+// each query stage.  dV CTAs lay out their own (below).  Warps: 0-7 elementwise
+// (two warpgroups, half of the tile columns each), 8 TMA, 9 MMA.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -152,7 +154,7 @@ __device__ __forceinline__ void ld_shared_f4(uint32_t addr, float4& v) {
 __device__ __forceinline__ int first_qblock(const BwdArgs& a, int key0) {
   return a.causal ? max(0, key0 - (a.Nk - a.N)) / kBlk : 0;
 }
-// Blocks a CTA streams: for a dK or dV CTA the 64-row query blocks from its first
+// Blocks a CTA streams: for a dK CTA the 64-row query blocks from its first
 // visible one, over every query head of its group; for a dQ CTA the 64-key blocks
 // its rows see (0 when none: then it writes dQ = 0).
 __device__ __forceinline__ int cta_blocks(const BwdArgs& a, int role, int blk) {
@@ -165,8 +167,8 @@ template <int ROLE, bool BF16>
 __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                            const CUtensorMap* tm_do, const BwdArgs& args, int blk, int head,
                                            uint8_t* smem, uint32_t sbase, uint32_t tmem) {
-  constexpr bool kKeyRows = ROLE != kRoleDQ;  // keys on TMEM lanes (dK, dV CTAs)
-  constexpr bool kThree = ROLE != kRoleDV;    // S, dP and the gradient product
+  static_assert(ROLE != kRoleDV, "dV CTAs run bwd256_dv_cta");
+  constexpr bool kKeyRows = ROLE == kRoleDK;  // keys on TMEM lanes (dK CTA)
   auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
   auto sZ = [&](int s) -> uint32_t { return sbase + kSmZ + kT64 * s; };
   auto sW = [&](int s) -> uint32_t { return sbase + kSmW + kT64 * s; };
@@ -199,10 +201,8 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nit > 0) {
-      if constexpr (kThree) {
-        mbar_expect_tx(bar(kYFull), kT128);
-        load_tile128(sY, mY, bar(kYFull), row0, kKeyRows ? bh_kv : head, ext_y, args.err);
-      }
+      mbar_expect_tx(bar(kYFull), kT128);
+      load_tile128(sY, mY, bar(kYFull), row0, kKeyRows ? bh_kv : head, ext_y, args.err);
       int n_z = 0, n_w = 0;  // loads issued
       for (int it = 0; it < nit; ++it) {
         const int s = it % kZStages, u = it / kZStages;
@@ -224,7 +224,7 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
       }
       // Every copy this thread issued lands before the CTA exits, even when the
       // consumers gave up after a timeout elsewhere (bounded waits, abort ignored).
-      if constexpr (kThree) mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma, false);
+      mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma, false);
       for (int s = 0; s < kZStages; ++s)
         if (n_z > s) mbar_wait(bar(kZFull + s), ((n_z - 1 - s) / kZStages) & 1, args.err, kErrTimeoutTma, false);
       for (int s = 0; s < kWStages; ++s)
@@ -238,7 +238,7 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
       auto zfull = [&](int it) { return mbar_wait(bar(kZFull + it % kZStages), (it / kZStages) & 1, args.err, kErrTimeoutTma); };
       auto wfull = [&](int it) { return mbar_wait(bar(kWFull + it % kWStages), (it / kWStages) & 1, args.err, kErrTimeoutTma); };
       bool ok = mbar_wait(bar(kAReady), 0, args.err, kErrTimeoutSoftmax) && zfull(0);
-      if constexpr (kThree) {
+      {
         // Order: S(0) dP(0) | S(i+1) G(i) dP(i+1) | ...  S(i+1) follows the read-out of
         // S(i); dP(i+1) overwrites the packed dS(i) only after G(i) has read it (one
         // thread's tcgen05.mma operations execute in issue order).
@@ -273,41 +273,11 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
             mma_commit(bar(kWEmpty + (it + 1) % kWStages));
           }
         }
-      } else {
-        // dV: S^T(0) S^T(1) | dV(i) S^T(i+2) | ...  S^T(i+2) overwrites the packed P^T(i)
-        // only after dV(i) has read it.
-        if (ok) {
-          tc_fence_after();
-          score_ts(tB0, tA, sZ(0), kIdS);
-          mma_commit(bar(kSReady + 0));
-          if (nit > 1) {
-            if ((ok = zfull(1))) {
-              tc_fence_after();
-              score_ts(tB1, tA, sZ(1), kIdS);
-              mma_commit(bar(kSReady + 1));
-            }
-          }
-        }
-        for (int it = 0; ok && it < nit; ++it) {
-          const int b = it & 1;
-          const uint32_t tBuf = b ? tB1 : tB0;
-          if (!(ok = mbar_wait(bar(kPFull + b), (it >> 1) & 1, args.err, kErrTimeoutSoftmax) && wfull(it))) break;
-          tc_fence_after();
-          grad_ts(tG, tBuf, sW(it % kWStages), kIdG, it > 0);
-          mma_commit(bar(kWEmpty + it % kWStages));  // dO(it): read by dV(it)
-          mma_commit(bar(kZEmpty + it % kZStages));  // Q(it) and its L, D: done with block it
-          if (it + 2 < nit) {
-            if (!(ok = zfull(it + 2))) break;
-            tc_fence_after();
-            score_ts(tBuf, tA, sZ((it + 2) % kZStages), kIdS);
-            mma_commit(bar(kSReady + b));
-          }
-        }
       }
       mma_commit(bar(kDone));  // also ends the epilogue's wait after a failure (result discarded)
       mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
     }
-  } else {
+  } else if (warp < kEwWarps) {
     // ------------------------------------------------------------ elementwise warps + epilogue
     const int e = warp >> 2;                 // warpgroup: tile columns [32 e, 32 e + 32)
     const int r = ((warp & 3) << 5) + lane;  // TMEM lane: key row (dK, dV) or query row (dQ)
@@ -347,7 +317,7 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
     }
     const int cbeg = 32 * e;
     for (int it = 0; ok && it < nit; ++it) {
-      const int c0 = z_row(it);  // first query (dK, dV) or key (dQ) of the block
+      const int c0 = z_row(it);  // first query (dK) or key (dQ) of the block
       // some visible (key, query) pair hidden in this block: causal diagonal, or (dQ)
       // keys past N_k in the last block (their K, V rows are zero, but P would not be)
       const bool diag = kKeyRows ? (args.causal && row0 + kRes - 1 > c0 + koff)
@@ -362,16 +332,13 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
           float4 t;
           ld_shared_f4(sLD(s) + 4u * (cbeg + 4 * i), t);
           l4v[4 * i] = t.x, l4v[4 * i + 1] = t.y, l4v[4 * i + 2] = t.z, l4v[4 * i + 3] = t.w;
-          if constexpr (kThree) {
-            ld_shared_f4(sLD(s) + 256u + 4u * (cbeg + 4 * i), t);
-            d4v[4 * i] = t.x, d4v[4 * i + 1] = t.y, d4v[4 * i + 2] = t.z, d4v[4 * i + 3] = t.w;
-          }
+          ld_shared_f4(sLD(s) + 256u + 4u * (cbeg + 4 * i), t);
+          d4v[4 * i] = t.x, d4v[4 * i + 1] = t.y, d4v[4 * i + 2] = t.z, d4v[4 * i + 3] = t.w;
         }
       }
       // ---- P = 2^(S c - L log2 e)
-      const int b = kThree ? 0 : (it & 1);
-      const uint32_t tS = tmem + lane_base + (b ? kTmBuf1 : kTmBuf0) + cbeg;
-      if (!(ok = warp_wait(bar(kSReady + b), kThree ? (it & 1) : ((it >> 1) & 1), args.err, kErrTimeoutMma))) break;
+      const uint32_t tS = tmem + lane_base + kTmBuf0 + cbeg;
+      if (!(ok = warp_wait(bar(kSReady), it & 1, args.err, kErrTimeoutMma))) break;
       tc_fence_after();
       uint32_t sv[32];
       tmem_ld_32x32b_x32(tS, sv);
@@ -397,16 +364,7 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
           if (hidden) p[x] = 0.f;
         }
       }
-      if constexpr (!kThree) {
-        // dV CTA: P^T packed back into the first 16 columns of this warpgroup's part
-        uint32_t pw[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) pw[x] = pack2<BF16>(p[2 * x], p[2 * x + 1]);
-        tmem_st_32x32b_x16(tS, pw);
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(bar(kPFull + b));
-      } else {
+      {
         tc_fence_before();
         warp_arrive(bar(kSFree));  // the scores may be overwritten by the next block's now
         // ---- dS = P o (dP - D), packed into the dP buffer
@@ -437,8 +395,8 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
     // [128 e, 128 e + 128).  A dQ CTA whose rows see no key writes dQ = 0.
     if (nit == 0 || (ok && warp_wait(bar(kDone), 0, args.err, kErrTimeoutMma))) {
       tc_fence_after();
-      const float mul = ROLE == kRoleDV ? 1.f : args.scale;
-      void* out = ROLE == kRoleDK ? args.dk : (ROLE == kRoleDV ? args.dv : args.dq);
+      const float mul = args.scale;
+      void* out = ROLE == kRoleDK ? args.dk : args.dq;
       uint16_t* dst = reinterpret_cast<uint16_t*>(out) + ((size_t)plane_a * nrows + row) * 256 + 128 * e;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -464,12 +422,269 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
   }
 }
 
-// FA_DEBUG builds: the phases every barrier of a CTA completed, against its
-// protocol (thread 0, after the CTA's final barrier, when no wait gave up).
+// ---------------------------------------------------------------- dV CTAs
+// A dV CTA has only the score product and dV, so it can stream 128-row query tiles:
+// K stays in shared memory (64 KB) as the A operand of S^T = K Q^T (N = 128), and
+// tensor memory holds S^T (columns 0-127), P^T packed (128-191) and dV (256-511).
+// With P^T apart from S^T, S^T(i+1) is issued as soon as the elementwise warps have
+// read S^T(i) and runs while they exponentiate; P^T(i+1) waits only for dV(i).  The
+// ring of two 64 KB slots is filled in the order the products read it: Q_0, Q_1,
+// dO_0, Q_2, dO_1, ..., dO_last; the L log2 e values of each query tile go through
+// two stages of their own (their reader, not the ring, decides when they are free).
+constexpr int kDvRows = 128;                  // query rows per streamed tile
+constexpr uint32_t kSmDvRing = kSmZ;          // two 64 KB slots
+constexpr uint32_t kTmDvS = 0, kTmDvP = 128;  // S^T fp32, P^T packed
+// barrier indices of the dV program (its own set in the same barrier array)
+enum : int {
+  kDvKFull = 0,    // K tile
+  kDvFull = 1,     // two ring slots
+  kDvEmpty = 3,    // two
+  kDvLFull = 5,    // two: L log2 e of block i in stage i & 1
+  kDvLEmpty = 7,   // two: the elementwise warps have read that stage
+  kDvSReady = 9,   // S^T in TMEM
+  kDvSFree = 10,   // S^T read out
+  kDvPFull = 11,   // P^T packed
+  kDvDone = 12,    // dV(i) has run: P^T may be overwritten
+  kDvDrain = 13,   // the last dV product has completed
+  kDvNumBars
+};
+static_assert(kDvNumBars <= kNumBars, "dV barriers inside the barrier array");
+static_assert(kSmDvRing + 2 * kT128 <= kSmLD, "dV ring inside the streamed-tile region");
+__device__ __forceinline__ void init_dv_barriers(uint32_t sbase) {
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  mbar_init(bar(kDvKFull), 1);
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(bar(kDvFull + s), 1);
+    mbar_init(bar(kDvEmpty + s), 1);
+    mbar_init(bar(kDvLFull + s), 1);
+    mbar_init(bar(kDvLEmpty + s), kEwWarps);
+  }
+  mbar_init(bar(kDvSReady), 1);
+  mbar_init(bar(kDvSFree), kEwWarps);
+  mbar_init(bar(kDvPFull), kEwWarps);
+  mbar_init(bar(kDvDone), 1);
+  mbar_init(bar(kDvDrain), 1);
+}
+
+__device__ __forceinline__ int dv_first_qblock(const BwdArgs& a, int key0) {
+  return a.causal ? max(0, key0 - (a.Nk - a.N)) / kDvRows : 0;
+}
+__device__ __forceinline__ int dv_blocks(const BwdArgs& a, int blk) {
+  return ((a.N + kDvRows - 1) / kDvRows - dv_first_qblock(a, blk * kRes)) * a.group;
+}
+// Ring item e: is it a dO tile, and of which block.  Q_0 | Q_{i+1}, dO_i | dO_last.
+__device__ __forceinline__ int dv_item(int e, int nit, bool& is_do) {
+  if (e == 0) { is_do = false; return 0; }
+  if (e == 2 * nit - 1) { is_do = true; return nit - 1; }
+  is_do = !(e & 1);
+  return (e & 1) ? (e + 1) >> 1 : (e >> 1) - 1;
+}
+// Acc (128 x 128) = A B^T, A and B 128-row K-major tiles in shared memory (d = 256).
+__device__ __forceinline__ void score_ss128(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
+  const uint32_t a0 = sdesc_lo(a_smem, 16), b0 = sdesc_lo(b_smem, 16);
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kP128 + (kk & 3) * 32) >> 4;
+    mma_ss_lohi(d_tmem, a0 + off, kHi, b0 + off, kHi, idesc, kk > 0);
+  }
+}
+// Acc (128 x 256) (+)= A B, A (128 x 128) packed in TMEM, B a 128-row tile read MN-major.
+__device__ __forceinline__ void grad_ts128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc, bool acc) {
+  const uint32_t b0 = sdesc_lo(b_smem, kP128);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_lohi(d_tmem, a_tmem + 8 * kk, b0 + ((kk * 2048) >> 4), kHi, idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void bwd256_dv_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_do, const BwdArgs& args, int blk, int head,
+                                              uint32_t sbase, uint32_t tmem) {
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  auto sRing = [&](int s) -> uint32_t { return sbase + kSmDvRing + kT128 * s; };
+  auto sL = [&](int i) -> uint32_t { return sbase + kSmLD + 512u * (i & 1); };  // L log2 e of block i
+  const uint32_t sK = sbase + kSmY;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N, Nk = args.Nk;
+  const int koff = Nk - N;
+  const int key0 = blk * kRes;
+  const int nit = dv_blocks(args, blk);  // >= 1: the last query row sees every key
+  const int i_begin = dv_first_qblock(args, key0);
+  const int nit_h = (N + kDvRows - 1) / kDvRows - i_begin;
+  const int hpb = args.H / args.group;
+  const int bh_q0 = (head / hpb) * args.H + (head % hpb) * args.group;
+  auto q_row = [&](int i) { return (i_begin + i % nit_h) * kDvRows; };
+  auto q_plane = [&](int i) { return bh_q0 + i / nit_h; };
+  const Extent3 ext_q{256, N, args.BH}, ext_kv{256, Nk, args.BHkv};
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(kDvKFull), kT128);
+      load_tile128(sK, tm_k, bar(kDvKFull), key0, head, ext_kv, args.err);
+      int n = 0, nl = 0;  // ring loads and L loads issued
+      for (int e = 0; e < 2 * nit; ++e) {
+        const int s = e & 1, u = e >> 1;
+        if (u > 0 && !mbar_wait(bar(kDvEmpty + s), (u - 1) & 1, args.err, kErrTimeoutRing)) break;
+        bool is_do;
+        const int i = dv_item(e, nit, is_do);
+        mbar_expect_tx(bar(kDvFull + s), kT128);
+        load_tile128(sRing(s), is_do ? tm_do : tm_q, bar(kDvFull + s), q_row(i), q_plane(i), ext_q, args.err);
+        ++n;
+        if (!is_do) {
+          // L log2 e of block i into stage i & 1, once the elementwise warps have read block i - 2's
+          const int b = i & 1;
+          if (i >= 2 && !mbar_wait(bar(kDvLEmpty + b), ((i >> 1) - 1) & 1, args.err, kErrTimeoutRing)) break;
+          const long long nrows = (long long)args.BH * args.Npad, first = (long long)q_plane(i) * args.Npad + q_row(i);
+          mbar_expect_tx(bar(kDvLFull + b), 512);
+          bulk_load_rows(sL(i), args.lse_log2, first, 512, nrows, bar(kDvLFull + b), args.err);
+          ++nl;
+        }
+      }
+      // Every copy this thread issued lands before the CTA exits (bounded waits, abort ignored).
+      mbar_wait(bar(kDvKFull), 0, args.err, kErrTimeoutTma, false);
+      for (int s = 0; s < 2; ++s) {
+        if (n > s) mbar_wait(bar(kDvFull + s), ((n - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
+        if (nl > s) mbar_wait(bar(kDvLFull + s), ((nl - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // S^T(0) | S^T(i+1) once S^T(i) has been read, then dV(i) once P^T(i) is packed | ...
+    // S^T(i+1) is issued after dV(i-1), so a dV(i) commit is at most one phase ahead
+    // of the elementwise warps that wait for it.
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_f16(BF16, 128, kDvRows, false, false);
+      constexpr uint32_t kIdG = idesc_grad(BF16);
+      auto full = [&](int e) { return mbar_wait(bar(kDvFull + (e & 1)), (e >> 1) & 1, args.err, kErrTimeoutTma); };
+      bool ok = mbar_wait(bar(kDvKFull), 0, args.err, kErrTimeoutTma) && full(0);
+      if (ok) {
+        tc_fence_after();
+        score_ss128(tmem + kTmDvS, sK, sRing(0), kIdS);
+        mma_commit(bar(kDvSReady));
+        mma_commit(bar(kDvEmpty + 0));
+      }
+      for (int i = 0; ok && i < nit; ++i) {
+        if (i + 1 < nit) {
+          const int e = 2 * i + 1;  // Q_{i+1}
+          if (!(ok = mbar_wait(bar(kDvSFree), i & 1, args.err, kErrTimeoutSoftmax) && full(e))) break;
+          tc_fence_after();
+          score_ss128(tmem + kTmDvS, sK, sRing(e & 1), kIdS);
+          mma_commit(bar(kDvSReady));
+          mma_commit(bar(kDvEmpty + (e & 1)));
+        }
+        const int e = (i == nit - 1) ? 2 * nit - 1 : 2 * i + 2;  // dO_i
+        if (!(ok = full(e) && mbar_wait(bar(kDvPFull), i & 1, args.err, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        grad_ts128(tmem + kTmG, tmem + kTmDvP, sRing(e & 1), kIdG, i > 0);
+        mma_commit(bar(kDvDone));
+        mma_commit(bar(kDvEmpty + (e & 1)));
+      }
+      mma_commit(bar(kDvDrain));  // also ends the epilogue's wait after a failure (result discarded)
+      mbar_wait(bar(kDvDrain), 0, args.err, kErrTimeoutMma, false);
+    }
+  } else if (warp < kEwWarps) {
+    // ------------------------------------------------------------ P^T, epilogue
+    const int e = warp >> 2;                 // warpgroup: query columns [64 e, 64 e + 64)
+    const int r = ((warp & 3) << 5) + lane;  // TMEM lane: key row
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int key = key0 + r;
+    const float c = args.scale_log2;
+    bool ok = true;
+    for (int i = 0; ok && i < nit; ++i) {
+      const int q0 = q_row(i);
+      const bool diag = args.causal && key0 + kRes - 1 > q0 + koff;  // some key hidden from some query
+      // L log2 e of the block's queries, in stage i & 1 (the stage's barrier is at most
+      // one phase ahead: block i + 2's copy waits for this block's LEmpty)
+      if (!(ok = warp_wait(bar(kDvLFull + (i & 1)), (i >> 1) & 1, args.err, kErrTimeoutTma))) break;
+      float lv[64];
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        float4 t;
+        ld_shared_f4(sL(i) + 4u * (64 * e + 4 * x), t);
+        lv[4 * x] = t.x, lv[4 * x + 1] = t.y, lv[4 * x + 2] = t.z, lv[4 * x + 3] = t.w;
+      }
+      warp_arrive(bar(kDvLEmpty + (i & 1)));
+      if (!(ok = warp_wait(bar(kDvSReady), i & 1, args.err, kErrTimeoutMma))) break;
+      tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld_32x32b_x32(tmem + lane_base + kTmDvS + 64 * e, sv[0]);
+      tmem_ld_32x32b_x32(tmem + lane_base + kTmDvS + 64 * e + 32, sv[1]);
+      tmem_wait_ld();
+      reg_fence32(sv[0]);
+      reg_fence32(sv[1]);
+      tc_fence_before();
+      warp_arrive(bar(kDvSFree));  // S^T may be overwritten by the next block's scores now
+      float p[64];
+#pragma unroll
+      for (int x = 0; x < 64; x += 2) {
+        float x0, x1;
+        fma2v(__uint_as_float(sv[x >> 5][x & 31]), __uint_as_float(sv[x >> 5][(x & 31) + 1]), c, -lv[x], -lv[x + 1],
+              x0, x1);
+        p[x] = ex2_approx(x0);
+        p[x + 1] = ex2_approx(x1);
+      }
+      if (diag) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (key > q0 + 64 * e + x + koff) p[x] = 0.f;
+      }
+      // P^T(i) overwrites P^T(i-1): wait until dV(i-1) has read it
+      if (i > 0) {
+        if (!(ok = warp_wait(bar(kDvDone), (i - 1) & 1, args.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+      }
+      uint32_t pw[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) pw[x] = pack2<BF16>(p[2 * x], p[2 * x + 1]);
+      tmem_st_32x32b_x32(tmem + lane_base + kTmDvP + 32 * e, pw);
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(bar(kDvPFull));
+    }
+    // ---- dV rows: lane r holds key row `key`; warpgroup e writes columns [128 e, 128 e + 128)
+    if (ok && warp_wait(bar(kDvDrain), 0, args.err, kErrTimeoutMma)) {
+      tc_fence_after();
+      uint16_t* dst = reinterpret_cast<uint16_t*>(args.dv) + ((size_t)head * Nk + key) * 256 + 128 * e;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmG + 128 * e + 32 * ch, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        if (key < Nk) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8)
+            st_global_v4(dst + 32 * ch + x, pack2<BF16>(__uint_as_float(v[x]), __uint_as_float(v[x + 1])),
+                         pack2<BF16>(__uint_as_float(v[x + 2]), __uint_as_float(v[x + 3])),
+                         pack2<BF16>(__uint_as_float(v[x + 4]), __uint_as_float(v[x + 5])),
+                         pack2<BF16>(__uint_as_float(v[x + 6]), __uint_as_float(v[x + 7])));
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void check_phases_dv(uint32_t sbase, int nit, uint32_t* err) {
+  auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
+  check_phase(bar(kDvKFull), 1, err, kDvKFull);
+  for (int s = 0; s < 2; ++s) {
+    check_phase(bar(kDvFull + s), nit, err, kDvFull + s);  // 2 nit items alternate the two slots
+    check_phase(bar(kDvEmpty + s), nit, err, kDvEmpty + s);
+    check_phase(bar(kDvLFull + s), count_mod(nit, s, 2), err, kDvLFull + s);
+    check_phase(bar(kDvLEmpty + s), count_mod(nit, s, 2), err, kDvLEmpty + s);
+  }
+  for (int b : {kDvSReady, kDvSFree, kDvPFull, kDvDone}) check_phase(bar(b), nit, err, b);
+  check_phase(bar(kDvDrain), 1, err, kDvDrain);
+}
+
+// FA_DEBUG builds: the phases every barrier of a dK or dQ CTA completed, against
+// its protocol (thread 0, after the CTA's final barrier, when no wait gave up).
 template <int ROLE>
 __device__ __forceinline__ void check_phases(uint32_t sbase, int nit, uint32_t* err) {
   auto bar = [&](int i) -> uint32_t { return sbase + kSmBar + 8u * i; };
-  check_phase(bar(kYFull), ROLE != kRoleDV && nit > 0, err, kYFull);
+  check_phase(bar(kYFull), nit > 0, err, kYFull);
   check_phase(bar(kAReady), nit > 0, err, kAReady);
   for (int s = 0; s < kZStages; ++s) {
     check_phase(bar(kZFull + s), count_mod(nit, s, kZStages), err, kZFull + s);
@@ -479,14 +694,7 @@ __device__ __forceinline__ void check_phases(uint32_t sbase, int nit, uint32_t* 
     check_phase(bar(kWFull + s), count_mod(nit, s, kWStages), err, kWFull + s);
     check_phase(bar(kWEmpty + s), count_mod(nit, s, kWStages), err, kWEmpty + s);
   }
-  if (ROLE == kRoleDV) {
-    for (int b = 0; b < 2; ++b) {
-      check_phase(bar(kSReady + b), count_mod(nit, b, 2), err, kSReady + b);
-      check_phase(bar(kPFull + b), count_mod(nit, b, 2), err, kPFull + b);
-    }
-  } else {
-    for (int b : {kSReady, kSFree, kDpReady, kDsFull}) check_phase(bar(b), nit, err, b);
-  }
+  for (int b : {kSReady, kSFree, kDpReady, kDsFull}) check_phase(bar(b), nit, err, b);
   check_phase(bar(kDone), nit > 0, err, kDone);
 }
 
@@ -533,7 +741,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     head = h0 * grp + (int)(t % nq_heads);
   }
 
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && role == kRoleDV) {
+    init_dv_barriers(sbase);
+    fence_mbar_init();
+  } else if (threadIdx.x == 0) {
     mbar_init(sbase + kSmBar + 8u * kYFull, 1);
     mbar_init(sbase + kSmBar + 8u * kAReady, kEwWarps);
     for (int s = 0; s < kZStages; ++s) {
@@ -573,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (role == kRoleDK)
     bwd256_cta<kRoleDK, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
   else if (role == kRoleDV)
-    bwd256_cta<kRoleDV, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
+    bwd256_dv_cta<BF16>(&tm_q, &tm_k, &tm_do, args, blk, head, sbase, tmem);
   else
     bwd256_cta<kRoleDQ, BF16>(&tm_q, &tm_k, &tm_v, &tm_do, args, blk, head, smem, sbase, tmem);
 
@@ -581,10 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if constexpr (kDebug) {
     if (threadIdx.x == 0 && no_abort(args.err)) {
-      const int nit = cta_blocks(args, role, blk);
-      if (role == kRoleDK) check_phases<kRoleDK>(sbase, nit, args.err);
-      else if (role == kRoleDV) check_phases<kRoleDV>(sbase, nit, args.err);
-      else check_phases<kRoleDQ>(sbase, nit, args.err);
+      if (role == kRoleDK) check_phases<kRoleDK>(sbase, cta_blocks(args, role, blk), args.err);
+      else if (role == kRoleDV) check_phases_dv(sbase, dv_blocks(args, blk), args.err);
+      else check_phases<kRoleDQ>(sbase, cta_blocks(args, role, blk), args.err);
     }
   }
   if (warp == kWarpMma) {
