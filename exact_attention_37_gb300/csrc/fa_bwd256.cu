@@ -41,7 +41,11 @@
 // 64-row stages of the operand read by the score and gradient products, two of
 // the operand read by the second product (32 KB each), and the L, D values of
 // each query stage.  dV CTAs lay out their own (below).  Warps: 0-7 elementwise
-// (two warpgroups, half of the tile columns each), 8 TMA, 9 MMA.
+// (two warpgroups, half of the tile columns each), 8 TMA, 9 MMA, 10 a second MMA
+// issuer in dK and dQ CTAs.  One thread issues a tcgen05.mma only about every 50
+// cycles, more than the 32 an N = 64 score product takes, so there warp 9 issues
+// the score products (S buffer, read only by the elementwise warps) and warp 10
+// the dP and gradient products (dP buffer, where dS is packed for the gradient).
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -58,7 +62,8 @@ constexpr uint32_t kT128 = 4 * kP128;        // 128 rows x 256 columns (64 KB)
 constexpr int kZStages = 3, kWStages = 2;
 constexpr int kEwWarps = 8;
 constexpr int kWarpTma = 8, kWarpMma = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kWarpMma2 = 10;  // dK and dQ CTAs: the second MMA issuer (idle in dV CTAs)
+constexpr int kThreads = 11 * 32;
 
 // shared memory
 constexpr uint32_t kSmY = 0;
@@ -230,24 +235,32 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
       for (int s = 0; s < kWStages; ++s)
         if (n_w > s) mbar_wait(bar(kWFull + s), ((n_w - 1 - s) / kWStages) & 1, args.err, kErrTimeoutTma, false);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kWarpMma: S(0) | S(i+1) once S(i) has been read out; it reads only the
+    // resident operand and Z.  Warp kWarpMma2: dP(0) | G(i) once dS(i) is packed,
+    // dP(i+1); dP(i+1) overwrites the packed dS(i) only after G(i) has read it (one
+    // thread's tcgen05.mma operations execute in issue order).  Z(i) is read by
+    // S(i) and G(i): its slot is free once both issuers have released it (each
+    // waits for Z(i) to land first, so its arrival belongs to that item's phase).
     if (lane == 0 && nit > 0) {
       constexpr uint32_t kIdS = idesc_score(BF16), kIdG = idesc_grad(BF16);
       const uint32_t tA = tmem + kTmA, tB0 = tmem + kTmBuf0, tB1 = tmem + kTmBuf1, tG = tmem + kTmG;
       auto zfull = [&](int it) { return mbar_wait(bar(kZFull + it % kZStages), (it / kZStages) & 1, args.err, kErrTimeoutTma); };
       auto wfull = [&](int it) { return mbar_wait(bar(kWFull + it % kWStages), (it / kWStages) & 1, args.err, kErrTimeoutTma); };
-      bool ok = mbar_wait(bar(kAReady), 0, args.err, kErrTimeoutSoftmax) && zfull(0);
-      {
-        // Order: S(0) dP(0) | S(i+1) G(i) dP(i+1) | ...  S(i+1) follows the read-out of
-        // S(i); dP(i+1) overwrites the packed dS(i) only after G(i) has read it (one
-        // thread's tcgen05.mma operations execute in issue order).
-        if (ok) {
+      bool ok = true;
+      if (warp == kWarpMma) {
+        ok = mbar_wait(bar(kAReady), 0, args.err, kErrTimeoutSoftmax);
+        for (int it = 0; ok && it < nit; ++it) {
+          if (it > 0 && !(ok = mbar_wait(bar(kSFree), (it - 1) & 1, args.err, kErrTimeoutSoftmax))) break;
+          if (!(ok = zfull(it))) break;
           tc_fence_after();
-          score_ts(tB0, tA, sZ(0), kIdS);
+          score_ts(tB0, tA, sZ(it % kZStages), kIdS);
           mma_commit(bar(kSReady));
-          ok = mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma) && wfull(0);
+          mma_commit(bar(kZEmpty + it % kZStages));
         }
+      } else {
+        ok = mbar_wait(bar(kYFull), 0, args.err, kErrTimeoutTma) && wfull(0);
         if (ok) {
           tc_fence_after();
           score_ss(tB1, sY, sW(0), kIdS);
@@ -255,13 +268,7 @@ __device__ __forceinline__ void bwd256_cta(const CUtensorMap* tm_q, const CUtens
           mma_commit(bar(kWEmpty + 0));  // W(0): read by dP(0) only
         }
         for (int it = 0; ok && it < nit; ++it) {
-          if (it + 1 < nit) {
-            if (!(ok = mbar_wait(bar(kSFree), it & 1, args.err, kErrTimeoutSoftmax) && zfull(it + 1))) break;
-            tc_fence_after();
-            score_ts(tB0, tA, sZ((it + 1) % kZStages), kIdS);
-            mma_commit(bar(kSReady));
-          }
-          if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax))) break;
+          if (!(ok = mbar_wait(bar(kDsFull), it & 1, args.err, kErrTimeoutSoftmax) && zfull(it))) break;
           tc_fence_after();
           grad_ts(tG, tB1, sZ(it % kZStages), kIdG, it > 0);
           mma_commit(bar(kZEmpty + it % kZStages));  // Z(it): last read by G(it)
@@ -749,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sbase + kSmBar + 8u * kAReady, kEwWarps);
     for (int s = 0; s < kZStages; ++s) {
       mbar_init(sbase + kSmBar + 8u * (kZFull + s), 1);
-      mbar_init(sbase + kSmBar + 8u * (kZEmpty + s), 1);
+      mbar_init(sbase + kSmBar + 8u * (kZEmpty + s), 2);  // read by both issuers' products
     }
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(sbase + kSmBar + 8u * (kWFull + s), 1);
@@ -762,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sbase + kSmBar + 8u * kSFree, kEwWarps);
     mbar_init(sbase + kSmBar + 8u * kDpReady, 1);
     mbar_init(sbase + kSmBar + 8u * kDsFull, kEwWarps);
-    mbar_init(sbase + kSmBar + 8u * kDone, 1);
+    mbar_init(sbase + kSmBar + 8u * kDone, 2);  // both issuers
     fence_mbar_init();
   }
   if (warp == kWarpMma) {

@@ -22,6 +22,11 @@
 //                 overwrites the TMEM columns of P_t only after P_t V_j has read
 //                 them, and while softmax warpgroup t works on one block the
 //                 tensor cores work on the other sub-tile.
+//   warp 4*NQ+2   (d = 64 only) second MMA issuer.  One thread issues a
+//                 tcgen05.mma only about every 50 cycles, more than the 32 an
+//                 N = 64 product takes, so at d = 64, where P has TMEM columns of
+//                 its own, warp 4*NQ+1 issues the score products and this warp the
+//                 P V products; the two share no TMEM columns.
 //   warps 4t..4t+3  softmax for query sub-tile t: thread r owns query row r and
 //                 TMEM lane r, so every row reduction stays inside one thread.
 //                 Scores are taken to base 2 with one FMA (scale*log2 e folded in),
@@ -58,6 +63,12 @@ struct FwdLayout {
   // its own 64 columns there instead of into its S columns, so S(j+1) may overwrite
   // S(j) as soon as the softmax has read it, not only after P(j) V has run.
   static constexpr bool kSepP = NQ == 2 && D == 64;
+  // MMA issuers.  One thread issues a tcgen05.mma only about every 50 cycles, and
+  // an N = 64 product executes in 32, so with separate P buffers (which leave the
+  // score products and the P V products no TMEM columns in common) one warp issues
+  // the score products and another the P V products.
+  static constexpr int kIssuers = kSepP ? 2 : 1;
+  static constexpr int kThreads = (4 * NQ + 1 + kIssuers) * 32;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kFull = 1;
@@ -83,13 +94,13 @@ struct FwdLayout {
 };
 
 template <int D, int NQ, int STAGES, bool BF16>
-__global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
+__global__ void __launch_bounds__(FwdLayout<D, NQ, STAGES>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdArgs args) {
   using L = FwdLayout<D, NQ, STAGES>;
   constexpr int kWarpTma = 4 * NQ;
-  constexpr int kWarpMma = 4 * NQ + 1;
+  constexpr int kWarpMma = 4 * NQ + 1;  // MMA issuer (separate P buffers: score products; P V in the next warp)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,7 +149,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
     for (int t = 0; t < NQ; ++t) mbar_init(bar(L::kODone + t), 1);
     if constexpr (L::kSepP)
       for (int t = 0; t < NQ; ++t) mbar_init(bar(L::kSFree + t), kBM / 32);
-    mbar_init(bar(L::kDrain), 1);
+    mbar_init(bar(L::kDrain), L::kIssuers);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -202,8 +213,8 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       for (int s = 0; s < STAGES; ++s)
         if (n > s) mbar_wait(bar(L::kFull + s), ((n - 1 - s) / STAGES) & 1, args.err, kErrTimeoutTma, false);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer(s)
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_f16(BF16, kBM, kBN, false, false);
       constexpr uint32_t kIdPV = make_idesc_f16(BF16, kBM, D, false, true);
@@ -228,21 +239,24 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       auto wait_full = [&](int e) -> bool {
         return mbar_wait(bar(L::kFull + e % STAGES), (e / STAGES) & 1, args.err, kErrTimeoutTma);
       };
-      bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
       if constexpr (L::kSepP) {
-        // S_0(0) S_1(0) | S_t(j+1) once the softmax has read S_t(j), then P_t(j) V_j |
-        // ...  Ring item of K(j+1): 2j + 1; of V_j: 2j + 2, or 2nb - 1 for the last.
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < NQ; ++t)
-            if (nblk[t] > 0) {
-              issue_s(t, t, 0);
-              mma_commit(bar(L::kSFull + t));
-            }
-          mma_commit(bar(L::kEmpty + 0));
-        }
-        for (int j = 0; ok && j < nb; ++j) {
-          if (j + 1 < nb) {
+        // Two issuers.  Warp kWarpMma: S_0(0), S_1(0), then S_t(j+1) once the softmax
+        // has read S_t(j), and it releases the K items.  Warp kWarpMma + 1: P_t(j) V_j
+        // once P_t(j) is packed, and it releases the V items.  Ring item of K(j+1):
+        // 2j + 1; of V_j: 2j + 2, or 2nb - 1 for the last.
+        bool ok = nb > 0;
+        if (warp == kWarpMma) {
+          ok = ok && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < NQ; ++t)
+              if (nblk[t] > 0) {
+                issue_s(t, t, 0);
+                mma_commit(bar(L::kSFull + t));
+              }
+            mma_commit(bar(L::kEmpty + 0));
+          }
+          for (int j = 0; ok && j + 1 < nb; ++j) {
             const int ek = 2 * j + 1;
             if (!(ok = wait_full(ek))) break;
             for (int t = 0; t < NQ; ++t)
@@ -255,19 +269,23 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
             if (!ok) break;
             mma_commit(bar(L::kEmpty + ek % STAGES));
           }
-          const int ev = (j == nb - 1) ? 2 * nb - 1 : 2 * j + 2;
-          if (!(ok = wait_full(ev))) break;
-          for (int t = 0; t < NQ; ++t)
-            if (j < nblk[t]) {
-              if (!(ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax))) break;
-              tc_fence_after();
-              issue_pv(t, t, ev % STAGES, j);
-              mma_commit(bar(L::kODone + t));
-            }
-          if (!ok) break;
-          mma_commit(bar(L::kEmpty + ev % STAGES));
+        } else {
+          for (int j = 0; ok && j < nb; ++j) {
+            const int ev = (j == nb - 1) ? 2 * nb - 1 : 2 * j + 2;
+            if (!(ok = wait_full(ev))) break;
+            for (int t = 0; t < NQ; ++t)
+              if (j < nblk[t]) {
+                if (!(ok = mbar_wait(bar(L::kPFull + t), j & 1, args.err, kErrTimeoutSoftmax))) break;
+                tc_fence_after();
+                issue_pv(t, t, ev % STAGES, j);
+                mma_commit(bar(L::kODone + t));
+              }
+            if (!ok) break;
+            mma_commit(bar(L::kEmpty + ev % STAGES));
+          }
         }
       } else if constexpr (NQ == 1) {
+        bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
         // S(0) S(1) | P(j) V_j, S(j+2) | ...: S(j+2) overwrites buffer j & 1 only after
         // P(j) V_j has read it (one thread's MMAs execute in issue order).  Ring item
         // of S(j): 0 for j = 0, else 2j - 1; of P(j) V_j: 2j + 2, or 2nb - 1 for the last.
@@ -302,6 +320,7 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
           }
         }
       } else {
+      bool ok = nb > 0 && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -398,43 +417,65 @@ __global__ void __launch_bounds__((4 * NQ + 2) * 32, 1)
       const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
       const float alpha = ex2_approx(fmaf(m, c, -mc));  // 0 when m = -inf
       // p = 2^(s c - m c): packed FMA for the exponent, ex2, packed adds for the row
-      // sum.  P goes into the first 64 columns of S_t (two 16-bit values per column),
-      // part of a row at a time so the packed words do not all stay live.
-      // d = 64 stores a quarter row at a time (fewer live registers; faster there),
-      // d = 128 half a row.
-      constexpr int kPE = D == 64 ? 32 : 64;  // elements of P per store
-      // With separate P buffers, P(j) overwrites P(j-1): wait until P(j-1) V has run.
-      // (S(j) was issued after P(j-2) V, so that phase has completed: the parity is
-      // unambiguous.)
+      // sum.  P (two 16-bit values per column) goes into its own 64 columns (separate
+      // P buffers) or into the first 64 columns of S_t, half a row at a time so the
+      // packed words do not all stay live.
       bool o_done = false;
-      if constexpr (L::kSepP) {
-        if (j > 0) {
-          ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
-          if (!ok) break;
-          tc_fence_after();
-          o_done = true;
-        }
-      }
       const uint32_t tP = L::kSepP ? tmem + lane_base + L::p_col(t) : tS;
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      if constexpr (L::kSepP) {
+        // P(j) overwrites P(j-1) in its own columns: wait until P(j-1) V has run,
+        // but only after the first half row of exponentials, which overlap that
+        // product.  (P(j) V cannot be issued before P(j) is packed, so ODone is at
+        // most one phase ahead of this wait: its parity is unambiguous.)
+        uint32_t pa[32], pb[32];
 #pragma unroll
-      for (int h = 0; h < 128 / kPE; ++h) {
-        uint32_t pw[kPE / 2];
-#pragma unroll
-        for (int i = kPE * h; i < kPE * h + kPE; i += 4) {
+        for (int i = 0; i < 64; i += 4) {
           float x0, x1, x2, x3;
           fma2(s[i], s[i + 1], c, -mc, x0, x1);
           fma2(s[i + 2], s[i + 3], c, -mc, x2, x3);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           add2(l0, l1, p0, p1);
           add2(l2, l3, p2, p3);
-          pw[(i % kPE) >> 1] = pack2<BF16>(p0, p1);
-          pw[((i % kPE) >> 1) + 1] = pack2<BF16>(p2, p3);
+          pa[i >> 1] = pack2<BF16>(p0, p1);
+          pa[(i >> 1) + 1] = pack2<BF16>(p2, p3);
         }
-        if constexpr (kPE == 64)
+        if (j > 0) {
+          ok = warp_wait(bar(L::kODone + t), (j - 1) & 1, args.err, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          o_done = true;
+        }
+        tmem_st_32x32b_x32(tP, pa);
+#pragma unroll
+        for (int i = 64; i < 128; i += 4) {
+          float x0, x1, x2, x3;
+          fma2(s[i], s[i + 1], c, -mc, x0, x1);
+          fma2(s[i + 2], s[i + 3], c, -mc, x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          add2(l0, l1, p0, p1);
+          add2(l2, l3, p2, p3);
+          pb[(i - 64) >> 1] = pack2<BF16>(p0, p1);
+          pb[((i - 64) >> 1) + 1] = pack2<BF16>(p2, p3);
+        }
+        tmem_st_32x32b_x32(tP + 32, pb);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int i = 64 * h; i < 64 * h + 64; i += 4) {
+            float x0, x1, x2, x3;
+            fma2(s[i], s[i + 1], c, -mc, x0, x1);
+            fma2(s[i + 2], s[i + 3], c, -mc, x2, x3);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            add2(l0, l1, p0, p1);
+            add2(l2, l3, p2, p3);
+            pw[(i % 64) >> 1] = pack2<BF16>(p0, p1);
+            pw[((i % 64) >> 1) + 1] = pack2<BF16>(p2, p3);
+          }
           tmem_st_32x32b_x32(tP + 32 * h, pw);
-        else
-          tmem_st_32x32b_x16(tP + 16 * h, pw);
+        }
       }
       l = l * alpha + ((l0 + l1) + (l2 + l3));
       tmem_wait_st();
@@ -553,7 +594,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   if (err != cudaSuccess) return err;
   const long long grid = (long long)a.num_qblocks * a.BH;
   profile_mark_begin(stream);
-  kern<<<(unsigned)grid, (4 * NQ + 2) * 32, L::kAlloc, stream>>>(q, k, v, o, a);
+  kern<<<(unsigned)grid, L::kThreads, L::kAlloc, stream>>>(q, k, v, o, a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   profile_mark_end(stream, kProfileFwd);
