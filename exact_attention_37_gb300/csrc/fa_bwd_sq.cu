@@ -30,7 +30,14 @@
 //
 // The score products have M = N = 128, the gradient products N = d.  Warps: 4 NWG
 // elementwise warps (NWG warpgroups, 128 / NWG tile columns each; every warp
-// arrives once on the barriers it signals), one TMA warp, one MMA warp.
+// arrives once on the barriers it signals), one TMA warp, one MMA warp, and in the
+// dQ kernel a second MMA warp.  One thread issues a tcgen05.mma only about every
+// 50 cycles, so the dQ kernel splits its products by the tensor-memory columns
+// they touch: S on one issuer, dP and dQ (which reads dS from the dP buffers) on
+// the other, so every product that overwrites columns another reads stays in the
+// same thread as its reader.  (The same split of the dK/dV kernel, S^T and dV |
+// dP^T and dK, interleaves the two streams so that S^T(i+1) lands later; it was
+// slower.)
 #include <algorithm>
 
 #include "fa_internal.h"
@@ -51,7 +58,9 @@ struct SqCfg {
   static constexpr int kEw = 128 * NWG;        // elementwise threads
   static constexpr int kWarpTma = 4 * NWG;
   static constexpr int kWarpMma = 4 * NWG + 1;
-  static constexpr int kThreads = kEw + 64;
+  static constexpr int kWarpMma2 = 4 * NWG + 2;  // dQ kernel: the second MMA issuer
+  static constexpr int kThreadsKV = kEw + 64;
+  static constexpr int kThreadsQ = kEw + 96;
   // TMEM column, relative to a packed region, of the 16 K elements of step kk:
   // warpgroup e packs its kCols columns into kCols / 2 columns starting at kCols e.
   static constexpr uint32_t packed_col(int kk) { return kCols * ((16 * kk) / kCols) + ((16 * kk) % kCols) / 2; }
@@ -149,7 +158,7 @@ constexpr uint32_t tm_dk() { return 256 + D; }
 }  // namespace kv
 
 template <int D, int NWG, bool BF16>
-__global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
+__global__ void __launch_bounds__(SqCfg<NWG>::kThreadsKV, 1)
     fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdArgs args) {
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       if (!ok) mma_commit(bar(kDone));  // lets the epilogue wait end; its result is discarded
       mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
     }
-  } else {
+  } else if (warp < 4 * NWG) {
     // ------------------------------------------------------------ P^T, dS^T, epilogue
     const int e = warp >> 2;                 // warpgroup: query columns [kCols e, kCols (e + 1))
     const int r = ((warp & 3) << 5) + lane;  // TMEM lane: key row
@@ -467,7 +476,7 @@ constexpr uint32_t kTmDQ = 384;
 }  // namespace qk
 
 template <int D, int NWG, bool BF16>
-__global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
+__global__ void __launch_bounds__(SqCfg<NWG>::kThreadsQ, 1)
     fa_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdArgs args) {
@@ -509,7 +518,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
     mbar_init(bar(kQFull), 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar(kKFull + s), 1);
-      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kKEmpty + s), 2);  // K: read by S and dQ, one issuer each
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kVFull + s), 1);
@@ -521,7 +530,7 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       mbar_init(bar(kDpReady + b), 1);
       mbar_init(bar(kDsFull + b), C::kEw / 32);
     }
-    mbar_init(bar(kDone), 1);
+    mbar_init(bar(kDone), 2);  // both issuers
     fence_mbar_init();
   }
   if (warp == C::kWarpMma) {
@@ -566,47 +575,50 @@ __global__ void __launch_bounds__(SqCfg<NWG>::kThreads, 1)
       for (int s = 0; s < 2; ++s)
         if (n_v > s) mbar_wait(bar(kVFull + s), ((n_v - 1 - s) >> 1) & 1, args.err, kErrTimeoutTma, false);
     }
-  } else if (warp == C::kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order: S(0) dP(0) dP(1) | S(j+1) dQ(j) dP(j+2) | ...  S(j+1) follows as soon as
-    // S(j) has been read out; dP(j+2) goes into the buffer of block j, whose dS(j)
-    // dQ(j) has just read (one thread's tcgen05.mma operations execute in issue
-    // order), so dP runs two blocks ahead of the elementwise warps.
+  } else if (warp == C::kWarpMma || warp == C::kWarpMma2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kWarpMma: S(j), as soon as S(j-1) has been read out.  Warp kWarpMma2:
+    // dP(0) dP(1) | dQ(j) dP(j+2) | ...: dP(j+2) goes into the buffer of block j,
+    // whose dS(j) dQ(j) has just read (one thread's operations execute in issue
+    // order).  K(j) is read by S(j) and dQ(j): its slot is free once both issuers
+    // have released it (each waits for it to land first).
     if (lane == 0 && nkv > 0) {
-      constexpr uint32_t kIdG = kIdTS(BF16, D);
-      auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(bar(kKFull + j % 3), (j / 3) & 1, args.err, kErrTimeoutTma)) return false;
-        tc_fence_after();
-        mma_scores<D>(tmem + kTmS, sQ, sK(j % 3), kIdSS(BF16));
-        mma_commit(bar(kSReady));
-        return true;
-      };
-      auto issue_dp = [&](int j) -> bool {
-        if (!mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, args.err, kErrTimeoutTma)) return false;
-        tc_fence_after();
-        mma_scores<D>(tmem + kTmDP + 128 * (j & 1), sDO, sV(j & 1), kIdSS(BF16));
-        mma_commit(bar(kDpReady + (j & 1)));
-        mma_commit(bar(kVEmpty + (j & 1)));
-        return true;
-      };
       bool ok = mbar_wait(bar(kQFull), 0, args.err, kErrTimeoutTma);
-      if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
-      if (ok && nkv > 1) ok = issue_dp(1);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int b = j & 1;
-        if (!(ok = mbar_wait(bar(kPDone), j & 1, args.err, kErrTimeoutSoftmax))) break;
-        if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(bar(kDsFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax))) break;
-        tc_fence_after();
-        mma_packed<NWG>(tmem + kTmDQ, tmem + kTmDP + 128 * b, sK(j % 3), kIdG, j > 0);
-        mma_commit(bar(kKEmpty + j % 3));  // K(j): last read by dQ(j)
-        if (j + 2 < nkv && !(ok = issue_dp(j + 2))) break;
+      auto kfull = [&](int j) { return mbar_wait(bar(kKFull + j % 3), (j / 3) & 1, args.err, kErrTimeoutTma); };
+      if (warp == C::kWarpMma) {
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j > 0 && !(ok = mbar_wait(bar(kPDone), (j - 1) & 1, args.err, kErrTimeoutSoftmax))) break;
+          if (!(ok = kfull(j))) break;
+          tc_fence_after();
+          mma_scores<D>(tmem + kTmS, sQ, sK(j % 3), kIdSS(BF16));
+          mma_commit(bar(kSReady));
+          mma_commit(bar(kKEmpty + j % 3));
+        }
+      } else {
+        constexpr uint32_t kIdG = kIdTS(BF16, D);
+        auto issue_dp = [&](int j) -> bool {
+          if (!mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, args.err, kErrTimeoutTma)) return false;
+          tc_fence_after();
+          mma_scores<D>(tmem + kTmDP + 128 * (j & 1), sDO, sV(j & 1), kIdSS(BF16));
+          mma_commit(bar(kDpReady + (j & 1)));
+          mma_commit(bar(kVEmpty + (j & 1)));
+          return true;
+        };
+        if (ok) ok = issue_dp(0);
+        if (ok && nkv > 1) ok = issue_dp(1);
+        for (int j = 0; ok && j < nkv; ++j) {
+          const int b = j & 1;
+          if (!(ok = mbar_wait(bar(kDsFull + b), (j >> 1) & 1, args.err, kErrTimeoutSoftmax) && kfull(j))) break;
+          tc_fence_after();
+          mma_packed<NWG>(tmem + kTmDQ, tmem + kTmDP + 128 * b, sK(j % 3), kIdG, j > 0);
+          mma_commit(bar(kKEmpty + j % 3));
+          if (j + 2 < nkv && !(ok = issue_dp(j + 2))) break;
+        }
       }
       mma_commit(bar(kDone));
       mbar_wait(bar(kDone), 0, args.err, kErrTimeoutMma, false);
     }
-  } else {
+  } else if (warp < 4 * NWG) {
     // ------------------------------------------------------------ P, dS, epilogue
     const int e = warp >> 2;                 // warpgroup: key columns [kCols e, kCols (e + 1))
     const int r = ((warp & 3) << 5) + lane;  // TMEM lane: query row
@@ -727,7 +739,7 @@ template <int D, bool BF16>
 cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                       const BwdArgs& a, cudaStream_t stream) {
   constexpr int kNwg = FA_BWD_SQ_NWG;
-  constexpr int kThreads = SqCfg<kNwg>::kThreads;
+  constexpr int kThreadsKV = SqCfg<kNwg>::kThreadsKV, kThreadsQ = SqCfg<kNwg>::kThreadsQ;
   constexpr uint32_t kKvSmem = kv::smem_alloc<D>(), kQSmem = qk::smem_alloc<D>();
   auto kkv = fa_bwd_kv_kernel<D, kNwg, BF16>;
   auto kq = fa_bwd_q_kernel<D, kNwg, BF16>;
@@ -738,11 +750,11 @@ cudaError_t launch_sq(const CUtensorMap& q, const CUtensorMap& k, const CUtensor
   const long long grid_kv = (long long)((a.Nk + 127) / 128) * a.BHkv;
   const long long grid_q = (long long)((a.N + 127) / 128) * a.BH;
   profile_mark_begin(stream);
-  kkv<<<(unsigned)grid_kv, kThreads, kKvSmem, stream>>>(q, k, v, dout, a);
+  kkv<<<(unsigned)grid_kv, kThreadsKV, kKvSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   profile_mark_end(stream, kProfileBwdKV);
   profile_mark_begin(stream);
-  kq<<<(unsigned)grid_q, kThreads, kQSmem, stream>>>(q, k, v, dout, a);
+  kq<<<(unsigned)grid_q, kThreadsQ, kQSmem, stream>>>(q, k, v, dout, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   profile_mark_end(stream, kProfileBwdQ);
   return cudaSuccess;
