@@ -47,3 +47,24 @@ def test_random_problem_matches_oracle(seed):
     w = draw_case(seed)
     parity.check_forward_full(w)
     parity.check_backward_full(w)
+
+
+def draw_split_issuer_case(seed: int) -> Workload:
+    """Head dimensions 64 and 256 only: the kernels that issue their tensor-core
+    products from two warps (d = 64 forward; d = 256 dK and dQ CTAs; the dQ kernel
+    at every head dimension), with key counts that end some ring mid-phase."""
+    r = random.Random(seed)
+    d = r.choice([64, 256])
+    H = r.choice([1, 2, 4])
+    H_kv = r.choice([h for h in range(1, H + 1) if H % h == 0])
+    N = r.randint(1, 700)
+    N_k = N if r.random() < 0.4 else r.randint(1, 700)
+    return Workload(f"split{seed}_d{d}_H{H}_Hkv{H_kv}_N{N}_Nk{N_k}", 1, H, N, d, r.choice(["fp16", "bf16"]),
+                    r.random() < 0.5, r.choice([0.5, 1.0]), (seed, seed + 1, seed + 2, seed + 3), True, H_kv, N_k)
+
+
+@pytest.mark.parametrize("seed", [3000 + 29 * i for i in range(16)])
+def test_random_problem_split_issuer_kernels(seed):
+    w = draw_split_issuer_case(seed)
+    parity.check_forward_full(w)
+    parity.check_backward_full(w)
