@@ -246,7 +246,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   a.BH = (int)BH;
   a.H = H;
   a.group = H / H_kv;
-  const int rows = fwd_rows_per_cta(d);
+  const int rows = fwd_rows_per_cta(d, BH, N_q, sm_count());
   a.num_qblocks = (N_q + rows - 1) / rows;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
@@ -254,7 +254,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   a.head_group = cta_head_group(BH, a.num_qblocks, (size_t)4 * (N_q + N_k) * d, causal != 0);
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
-  cudaError_t e = launch_fwd(d, bf16, mq, mk, mv, mo, a, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd(d, bf16, rows, mq, mk, mv, mo, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

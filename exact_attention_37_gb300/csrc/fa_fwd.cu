@@ -603,15 +603,30 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
 
 }  // namespace
 
-int fwd_rows_per_cta(int d) { return d == 256 ? kBM : 2 * kBM; }
+int fwd_rows_per_cta(int d, long long BH, int N, int num_sms) {
+  if (d == 256) return kBM;
+  const long long ctas = BH * (((long long)N + 2 * kBM - 1) / (2 * kBM));
+  return ctas < num_sms ? kBM : 2 * kBM;
+}
 
-cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+// Two 128-row sub-tiles a CTA (eight softmax warps keep the MUFU and the tensor pipe
+// busy) unless the problem is too small to fill the GPU with such CTAs; then one
+// sub-tile a CTA with two score buffers, as at d = 256 (measured: faster for grids
+// under one wave, much slower for larger ones).
+cudaError_t launch_fwd(int d, bool bf16, int rows, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream) {
+  const bool one = rows == kBM;
   switch (d) {
     case 64:
+      if (one)
+        return bf16 ? launch_fwd_t<64, 1, 8, true>(q, k, v, o, a, stream)
+                    : launch_fwd_t<64, 1, 8, false>(q, k, v, o, a, stream);
       return bf16 ? launch_fwd_t<64, 2, 8, true>(q, k, v, o, a, stream)
                   : launch_fwd_t<64, 2, 8, false>(q, k, v, o, a, stream);
     case 128:
+      if (one)
+        return bf16 ? launch_fwd_t<128, 1, 5, true>(q, k, v, o, a, stream)
+                    : launch_fwd_t<128, 1, 5, false>(q, k, v, o, a, stream);
       return bf16 ? launch_fwd_t<128, 2, 5, true>(q, k, v, o, a, stream)
                   : launch_fwd_t<128, 2, 5, false>(q, k, v, o, a, stream);
     case 256:

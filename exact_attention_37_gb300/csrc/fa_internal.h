@@ -61,10 +61,13 @@ struct BwdArgs {
 // nblocks is the number of CTA blocks per head, each doing up to nblocks steps.
 int cta_head_group(long long nheads, int nblocks, size_t bytes_per_head, bool causal);
 
-// Rows of Q handled by one forward CTA for head dimension d.
-int fwd_rows_per_cta(int d);
+// Rows of Q handled by one forward CTA: 128 at d = 256; at d = 64 and 128, 256 (two
+// 128-row sub-tiles a CTA) unless that grid (BH x ceil(N / 256) CTAs) would fill less
+// than one wave of the num_sms SMs, then 128 (one sub-tile a CTA, twice the CTAs).
+int fwd_rows_per_cta(int d, long long BH, int N, int num_sms);
 
-cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+// Forward launch; `rows` is fwd_rows_per_cta's answer for the same problem.
+cudaError_t launch_fwd(int d, bool bf16, int rows, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdArgs& a, cudaStream_t stream);
 
 // Measurement hook: events around each main kernel launch while profiling is on
