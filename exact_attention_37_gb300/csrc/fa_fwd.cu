@@ -243,7 +243,10 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ, STAGES>::kThreads, 1)
         // Two issuers.  Warp kWarpMma: S_0(0), S_1(0), then S_t(j+1) once the softmax
         // has read S_t(j), and it releases the K items.  Warp kWarpMma + 1: P_t(j) V_j
         // once P_t(j) is packed, and it releases the V items.  Ring item of K(j+1):
-        // 2j + 1; of V_j: 2j + 2, or 2nb - 1 for the last.
+        // 2j + 1; of V_j: 2j + 2, or 2nb - 1 for the last.  The P V issuer's test of a
+        // V item's slot is never two phases stale: the slot last held either one of
+        // its own V items (seen in order) or a K item that an S(j') read before the
+        // P(j') this issuer has already waited for.
         bool ok = nb > 0;
         if (warp == kWarpMma) {
           ok = ok && mbar_wait(bar(L::kQFull), 0, args.err, kErrTimeoutTma) && wait_full(0);
