@@ -5,10 +5,12 @@ several 128-row tiles and a ragged tail.  The five workloads of the method's
 evaluation are run at full size in the launch configuration the bench uses and
 checked on sampled heads and rows.  Tolerances are in tests/parity.py.
 """
+import numpy as np
 import pytest
 import torch
 
 import exact_attention_37_gb300 as fa
+import oracle
 from exact_attention_37_gb300 import synth
 from exact_attention_37_gb300.synth import Workload
 
@@ -117,6 +119,29 @@ def test_ctx32k_backward_one_head():
     # on the GPU, the second checked in full against the oracle (row chunks)
     w = synth.CTX32K.with_(H=2, backward=True)
     parity.check_backward_sampled(w, [(0, 1)])
+
+
+def test_ctx128k_causal_forward_and_backward_sampled():
+    """N = 131072 (four times the longest workload), causal, two heads: sampled rows
+    of O and L, dQ of sampled rows, and dK, dV of the last 512 keys, which under the
+    causal mask only the last 512 queries see, so the oracle evaluates those rows
+    alone and still gives the exact gradients."""
+    N = 131072
+    w = synth.CTX32K.with_(name="ctx128k", H=2, N=N, backward=True)
+    q, k, v, do = synth.make_inputs(w, with_dout=True)
+    o, lse, dq, dk, dv = parity.run_backward(w, q, k, v, do)
+    o, lse, dq, dk, dv = (t.float().cpu() for t in (o, lse, dq, dk, dv))
+    rows = [0, 1, 4095, 65536, N - 513, N - 512, N - 1]
+    tail = np.arange(N - 512, N)
+    for h in (0, 1):
+        O_ref, L_ref = oracle.forward_rows(q[0, h], k[0, h], v[0, h], w.scale, True, rows)
+        parity.compare_o(w, o[0, h, rows].numpy().astype(np.float64), O_ref, f"O[0,{h}]")
+        parity.compare_l(lse[0, h, rows].numpy().astype(np.float64), L_ref)
+        rdq, _, _, _ = oracle.head_backward_rows(q[0, h], k[0, h], v[0, h], do[0, h], w.scale, True, rows)
+        parity.compare_g(dq[0, h, rows].numpy().astype(np.float64), rdq, f"dQ[0,{h}] rows")
+        _, rdk, rdv, _ = oracle.head_backward_rows(q[0, h], k[0, h], v[0, h], do[0, h], w.scale, True, tail)
+        parity.compare_g(dk[0, h, N - 512:].numpy().astype(np.float64), rdk[N - 512:], f"dK[0,{h}] last keys")
+        parity.compare_g(dv[0, h, N - 512:].numpy().astype(np.float64), rdv[N - 512:], f"dV[0,{h}] last keys")
 
 
 def test_forward_allocates_nothing_beyond_its_outputs():
