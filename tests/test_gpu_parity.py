@@ -144,6 +144,17 @@ def test_ctx128k_causal_forward_and_backward_sampled():
         parity.compare_g(dv[0, h, N - 512:].numpy().astype(np.float64), rdv[N - 512:], f"dV[0,{h}] last keys")
 
 
+@pytest.mark.parametrize("d,dtype,causal", [(64, "fp16", False), (128, "bf16", True), (256, "bf16", True)])
+def test_many_heads_short_sequences(d, dtype, causal):
+    """About a thousand heads of a few hundred rows (the ragged tail in every head):
+    the CTA order over head groups and the plane indexing at large B*H, checked on
+    heads spread over the batch (first, middle, last)."""
+    w = Workload(f"many_heads_d{d}", 32, 32, 130, d, dtype, causal, 1.0, (961, 962, 963, 964))
+    heads = [(0, 0), (15, 17), (31, 31)]
+    parity.check_forward_sampled(w, heads, list(range(0, 130, 7)) + [129])
+    parity.check_backward_sampled(w, heads)
+
+
 def test_forward_allocates_nothing_beyond_its_outputs():
     """O(N) memory: at N = 32768 a single fp32 score matrix of one head would take
     4.3 GB; the forward call's footprint is its two outputs (allocated by torch in
