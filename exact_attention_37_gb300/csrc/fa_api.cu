@@ -14,6 +14,7 @@
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
+#include "fa_marks.h"
 #include "fa_nvtx.h"
 #include "ptx.cuh"
 
@@ -182,7 +183,30 @@ void profile_mark_begin(cudaStream_t stream) {
   if (cudaEventRecord(p.ev[p.used].first, stream) == cudaSuccess) p.open = true;
 }
 
+namespace {
+// The host-buffer pipeline's dK/dV mark (one per thread: calls on other threads
+// are not affected).
+thread_local cudaEvent_t t_dkdv_mark = nullptr;
+thread_local bool t_dkdv_recorded = false;
+}  // namespace
+
+void arm_dkdv_mark(cudaEvent_t ev) {
+  t_dkdv_mark = ev;
+  t_dkdv_recorded = false;
+}
+
+bool take_dkdv_mark() {
+  const bool r = t_dkdv_recorded;
+  t_dkdv_mark = nullptr;
+  t_dkdv_recorded = false;
+  return r;
+}
+
 void profile_mark_end(cudaStream_t stream, int kind) {
+  if (t_dkdv_mark && (kind == kProfileBwdKV || kind == kProfileBwdFused)) {
+    t_dkdv_recorded = cudaEventRecord(t_dkdv_mark, stream) == cudaSuccess;
+    t_dkdv_mark = nullptr;
+  }
   Profile& p = profile();
   if (!p.on || !p.open) return;
   p.open = false;

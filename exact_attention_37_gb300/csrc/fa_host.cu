@@ -2,9 +2,10 @@
 // host memory, pipelined over chunks of heads on three library-owned streams so
 // that the host-to-device copies of chunk c + 1, the kernels of chunk c and the
 // device-to-host copies of chunk c - 1 overlap.  Within a chunk the forward pass
-// starts once Q, K and V are on the device (dO follows), and O and L go back as
-// soon as the forward pass has written them, so the pipeline's fill and drain
-// carry only part of a chunk's copies.  Heads are independent in both
+// starts once Q, K and V are on the device (dO follows); O and L go back as soon
+// as the forward pass has written them, and dK and dV as soon as the kernel that
+// writes them has run (while the dQ kernel runs), so the pipeline's fill and
+// drain carry only part of a chunk's copies.  Heads are independent in both
 // passes, so a chunk of heads is a complete problem of its own; each chunk runs
 // through fa_fwd_ex / fa_bwd_ex on a slice of one device scratch region that
 // the caller provides (the library allocates no device memory).
@@ -14,6 +15,7 @@
 
 #include "../../include/fa_attention.h"
 #include "fa_internal.h"
+#include "fa_marks.h"
 #include "fa_nvtx.h"
 
 namespace fa {
@@ -62,7 +64,7 @@ struct Pipeline {
   cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
   cudaEvent_t qkv_up[kMaxChunks] = {}, dout_up[kMaxChunks] = {};
-  cudaEvent_t fwd_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {};
+  cudaEvent_t fwd_done[kMaxChunks] = {}, dkdv_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {};
   bool ready = false;
 };
 
@@ -84,6 +86,7 @@ bool pipeline_for_device(Pipeline** out) {
       if (cudaEventCreateWithFlags(&p.qkv_up[c], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.dout_up[c], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.fwd_done[c], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.dkdv_done[c], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.comp_done[c], ef) != cudaSuccess)
         return false;
     p.ready = true;
@@ -202,17 +205,22 @@ fa_status enqueue_chunks(Pipeline* P, const ScratchLayout& L, char* s, const voi
     if (cudaEventRecord(P->fwd_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
     if (bwd) {
       if (cudaStreamWaitEvent(P->comp, P->dout_up[c], 0) != cudaSuccess) return FA_ERR_CUDA;
+      arm_dkdv_mark(P->dkdv_done[c]);  // recorded right after the kernel that writes dK and dV
       st = fa_bwd_ex(s + L.q + ot, s + L.k + ot, s + L.v + ot, s + L.o + ot, s + L.dout + ot,
                      reinterpret_cast<const float*>(s + L.lse + ol), s + L.dq + ot, s + L.dk + ot, s + L.dv + ot,
                      s + L.ws, L.ws_bytes, 1, hc, hc, N, N, d, scale, causal, dtype, cs);
+      const bool marked = take_dkdv_mark();
       if (st != FA_OK) return st;
       if (cudaEventRecord(P->comp_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
+      if (!marked && cudaEventRecord(P->dkdv_done[c], P->comp) != cudaSuccess) return FA_ERR_CUDA;
     }
-    // ---- download: O and L once the forward pass has written them, then the gradients
+    // ---- download: O and L once the forward pass has written them, dK and dV once
+    // their kernel has run, then dQ
     if (cudaStreamWaitEvent(P->down, P->fwd_done[c], 0) != cudaSuccess) return FA_ERR_CUDA;
     if (!D2H(o, L.o, ot, bt) || !D2H(lse, L.lse, ol, bl)) return FA_ERR_CUDA;
-    if (bwd && (cudaStreamWaitEvent(P->down, P->comp_done[c], 0) != cudaSuccess || !D2H(dq, L.dq, ot, bt) ||
-                !D2H(dk, L.dk, ot, bt) || !D2H(dv, L.dv, ot, bt)))
+    if (bwd && (cudaStreamWaitEvent(P->down, P->dkdv_done[c], 0) != cudaSuccess || !D2H(dk, L.dk, ot, bt) ||
+                !D2H(dv, L.dv, ot, bt) || cudaStreamWaitEvent(P->down, P->comp_done[c], 0) != cudaSuccess ||
+                !D2H(dq, L.dq, ot, bt)))
       return FA_ERR_CUDA;
   }
   return FA_OK;
