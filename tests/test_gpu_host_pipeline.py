@@ -1,6 +1,10 @@
 """The host-buffer entry points (head chunks pipelined over the library's streams)
-give the same results as the device entry points on the whole problem: bitwise
-for the deterministic d = 64 / 128 paths, whatever the chunk count.
+give the same results as the device entry points on the whole problem, bitwise
+(every path is deterministic), whatever the chunk count.  The device scratch is
+filled with 0xFF bytes (NaN in both 16-bit formats) before each call, so a copy
+to the host that started before the kernel writing its tensor had run (dK and dV
+go back while the dQ kernel runs) would show as NaN, not as an earlier call's
+identical result.
 """
 import pytest
 import torch
@@ -30,6 +34,10 @@ def built():
         # 35 heads of odd length: chunk starts must be multiples of 4 heads (L stays
         # 16-byte aligned); the default plan is 8, 12, 4, 11
         Workload("host_d64_35_heads", 5, 7, 33, 64, "fp16", True, 1.0, (713, 714, 715, 716)),
+        # kernels long enough that a download racing them would read unwritten scratch
+        Workload("host_d128_long", 1, 8, 2048, 128, "bf16", True, 1.0, (717, 718, 719, 720)),
+        # one launch writes dQ, dK and dV at d = 256
+        Workload("host_d256", 1, 3, 300, 256, "bf16", True, 1.0, (721, 722, 723, 724)),
     ],
     ids=lambda w: w.name,
 )
@@ -43,7 +51,7 @@ def test_host_pipeline_matches_device_path(w, chunks):
     qh, kh, vh, doh = (pin(x) for x in (q, k, v, do))
     oh, dqh, dkh, dvh = (torch.empty_like(x).pin_memory() for x in (q, q, k, v))
     lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    scratch = torch.empty(fa.fa_host_scratch_size(B, H, N, d, True), dtype=torch.uint8, device="cuda")
+    scratch = torch.full((fa.fa_host_scratch_size(B, H, N, d, True),), 0xFF, dtype=torch.uint8, device="cuda")
     fa.fa_fwd_bwd_host(qh, kh, vh, doh, oh, lseh, dqh, dkh, dvh, scratch, w.scale, w.causal, chunks)
     torch.cuda.current_stream().synchronize()
     fa.fa_check_device_status()
@@ -52,7 +60,7 @@ def test_host_pipeline_matches_device_path(w, chunks):
     # forward only
     oh2 = torch.empty_like(oh)
     lseh2 = torch.empty_like(lseh)
-    scratch_f = torch.empty(fa.fa_host_scratch_size(B, H, N, d, False), dtype=torch.uint8, device="cuda")
+    scratch_f = torch.full((fa.fa_host_scratch_size(B, H, N, d, False),), 0xFF, dtype=torch.uint8, device="cuda")
     fa.fa_fwd_host(qh, kh, vh, oh2, lseh2, scratch_f, w.scale, w.causal, chunks)
     torch.cuda.current_stream().synchronize()
     assert torch.equal(oh2, o_ref.cpu()) and torch.equal(lseh2, lse_ref.cpu())

@@ -68,8 +68,10 @@ def test_backward_small(d, dtype, causal):
 
 
 @pytest.mark.parametrize("N", [1, 64, 65, 127, 129, 200])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_ragged_lengths(N, d):
+    # d = 256 streams 64-row tiles in its dK and dQ CTAs and 128-row tiles in its dV
+    # CTAs, so 64, 65, 127 and 129 rows put a ragged tail in each
     parity.check_backward_full(small(N, d, "bf16", True, B=1, H=1))
 
 
