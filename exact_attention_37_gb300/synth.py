@@ -34,6 +34,7 @@ class Workload:
     backward: bool = True
     H_kv: int | None = None  # key/value heads (grouped-query attention); None means H
     N_k: int | None = None   # key/value rows; None means N
+    softmax_scale: float | None = None  # None means 1/sqrt(d)
 
     @property
     def kv_heads(self) -> int:
@@ -45,8 +46,9 @@ class Workload:
 
     @property
     def scale(self) -> float:
-        """Softmax scale 1/sqrt(d), rounded to float32 as the kernels receive it."""
-        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+        """Softmax scale (1/sqrt(d) unless set), rounded to float32 as the kernels receive it."""
+        s = 1.0 / math.sqrt(self.d) if self.softmax_scale is None else self.softmax_scale
+        return float(torch.tensor(s, dtype=torch.float32))
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -35,7 +35,7 @@ def test_grouped_query_forward_and_backward(H_kv, causal, d):
 
 @pytest.mark.parametrize("N,N_k", [(100, 300), (300, 100), (1, 257), (257, 1), (129, 640), (640, 129)])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_unequal_lengths_forward_and_backward(N, N_k, causal, d):
     w = w_ex(2, 1, N, N_k, d, "fp16", causal)
     parity.check_forward_full(w)

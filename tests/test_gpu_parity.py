@@ -75,6 +75,19 @@ def test_backward_ragged_lengths(N, d):
     parity.check_backward_full(small(N, d, "bf16", True, B=1, H=1))
 
 
+# --------------------------------------------------------------------- the softmax scale argument
+@pytest.mark.parametrize("scale", [0.03, 0.3, 1.0])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_softmax_scale_argument(d, scale):
+    # Every other case runs at 1/sqrt(d); here the kernels must take the scale they are
+    # given, in the exponent of P (forward and backward) and in dQ = scale dS K and
+    # dK = scale dS^T Q.  At 1.0 the rows are far from uniform (scores of spread sqrt(d)).
+    w = small(200, d, "bf16", True, H=2).with_(softmax_scale=scale, name=f"scale{scale}_d{d}")
+    parity.check_backward_full(w)
+    for causal in (True, False):
+        parity.check_forward_full(w.with_(causal=causal))
+
+
 # --------------------------------------------------------------------- the five workloads at full size
 def test_train_workload_forward_sampled():
     w = synth.TRAIN
