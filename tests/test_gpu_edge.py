@@ -6,6 +6,10 @@ key row past N_k in a ragged last block) would overflow.  Those keys are not
 part of the problem and must contribute nothing, not inf or NaN.  The inputs
 are seeded: K rows are all close to one direction u and some query rows point
 the other way, so their scores sit near -120.
+
+Rows whose scores rise steadily along the keys move the running maximum in every
+key block (the forward pass rescales O each time); falling rows keep the first
+block's maximum while every later exponential underflows.
 """
 import numpy as np
 import pytest
@@ -13,7 +17,7 @@ import torch
 
 import exact_attention_37_gb300 as fa
 import oracle
-from exact_attention_37_gb300.synth import DTYPES
+from exact_attention_37_gb300.synth import DTYPES, Workload
 
 from . import parity
 
@@ -58,6 +62,54 @@ def test_rows_with_very_negative_scores_and_a_ragged_key_tail(d, Nk):
     assert np.abs(O - O_ref).max() <= parity.O_ABS["bf16"]
     parity.compare_l(lse.cpu().numpy().astype(np.float64), L_ref)
     rdq, rdk, rdv, _ = oracle.attention_backward(q, k, v, do, scale, False)
+    parity.compare_g(parity.to_np(dq), rdq, "dQ")
+    parity.compare_g(parity.to_np(dk), rdk, "dK")
+    parity.compare_g(parity.to_np(dv), rdv, "dV")
+
+
+def ramp_scores(H, N, d, dtype, rising, seed):
+    """Scores that rise (or fall) steadily along the keys: q_i = sqrt(d) u + g_i,
+    k_j = 200 t_j u + 4 g'_j, u a unit vector, g, g' standard normal and t_j = j / N (or
+    1 - j / N), so scale * q.k spans about 200 across the row, with noise of about 4.
+    Rising, every 128-key block lifts the row maximum by about 40 (more than 50 in
+    base 2), so the running maximum moves in every block and O is rescaled each time;
+    falling, the first block holds the maximum and the later blocks' exponentials
+    underflow.  The noise in K is not decoration: with K rows that share one large
+    component (200 t_j u alone), dQ = scale dS K is a sum whose terms cancel to a few
+    parts in a thousand, and rounding dS to 16 bits before that product (as the method
+    does) leaves no correct digit; an fp64 emulation of that rounding shows the same
+    40 % error.  With the noise the emulation is within 1 %."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.ones(d) / d ** 0.5
+    t = torch.arange(N, dtype=torch.float32) / N
+    if not rising:
+        t = 1.0 - t
+    k = (200.0 * t)[None, None, :, None] * u + 4.0 * torch.randn(1, H, N, d, generator=g)
+    q = d ** 0.5 * u + torch.randn(1, H, N, d, generator=g)
+    v = torch.randn(1, H, N, d, generator=g)
+    do = torch.randn(1, H, N, d, generator=g)
+    return tuple(x.to(DTYPES[dtype]) for x in (q, k, v, do))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("rising", [True, False], ids=["rising", "falling"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_scores_that_move_the_running_maximum_every_block(d, rising, causal):
+    N = 700
+    q, k, v, do = ramp_scores(2, N, d, "bf16", rising, 700 + d + 2 * rising + causal)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, scale=scale, causal=causal)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, scale=scale, causal=causal)
+    fa.fa_check_device_status()
+    O_ref, L_ref = oracle.attention_forward(q, k, v, scale, causal)
+    if rising and not causal:
+        assert L_ref[0, 0, 0] > 150  # the row maximum really sits in the last block
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    parity.compare_o(Workload("ramp", 1, 2, N, d, "bf16", causal), parity.to_np(o), O_ref)
+    parity.compare_l(lse.cpu().numpy().astype(np.float64), L_ref)
+    rdq, rdk, rdv, _ = oracle.attention_backward(q, k, v, do, scale, causal)
     parity.compare_g(parity.to_np(dq), rdq, "dQ")
     parity.compare_g(parity.to_np(dk), rdk, "dK")
     parity.compare_g(parity.to_np(dv), rdv, "dV")
