@@ -68,3 +68,23 @@ def test_random_problem_split_issuer_kernels(seed):
     w = draw_split_issuer_case(seed)
     parity.check_forward_full(w)
     parity.check_backward_full(w)
+
+
+def draw_long_case(seed: int) -> Workload:
+    """Longer rows (600 to 2100 queries and keys): every ring and double buffer wraps
+    many times, and the unequal-length causal offset reaches whole blocks."""
+    r = random.Random(seed)
+    d = r.choice([64, 128, 256])
+    H = r.choice([1, 2])
+    H_kv = r.choice([h for h in range(1, H + 1) if H % h == 0])
+    N = r.randint(600, 2100)
+    N_k = N if r.random() < 0.5 else r.randint(300, 2100)
+    return Workload(f"long{seed}_d{d}_H{H}_Hkv{H_kv}_N{N}_Nk{N_k}", 1, H, N, d, r.choice(["fp16", "bf16"]),
+                    r.random() < 0.5, r.choice([0.5, 1.0]), (seed, seed + 1, seed + 2, seed + 3), True, H_kv, N_k)
+
+
+@pytest.mark.parametrize("seed", [5000 + 31 * i for i in range(12)])
+def test_random_longer_problem_matches_oracle(seed):
+    w = draw_long_case(seed)
+    parity.check_forward_full(w)
+    parity.check_backward_full(w)
