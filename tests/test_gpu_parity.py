@@ -170,6 +170,43 @@ def test_many_heads_short_sequences(d, dtype, causal):
     parity.check_backward_sampled(w, heads)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_tensors_past_two_to_the_31_elements(d):
+    """Every tensor holds more than 2^31 elements (about 4.3 GB each, some 35 GB in all
+    with the gradients): the element offset of head h is h N d, which passes 2^31 at
+    h* = 2^31 / (N d), so an index computed in 32-bit arithmetic anywhere (a pointer
+    offset, a tensor-map plane, a workspace row) would put the heads from h* on in the
+    wrong place.  Inputs are N(0, 1) drawn on the device from a seeded generator (a
+    host draw of this size takes minutes); the heads on both sides of h* and the last
+    one are copied back and checked in full, forward and backward, against the oracle."""
+    N = 1024
+    h_star = (1 << 31) // (N * d)
+    B, H = 2, h_star // 2 + 8  # B*H = h_star + 16 heads
+    torch.cuda.empty_cache()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(20000 + d)
+    q, k, v, do = (torch.randn(B, H, N, d, generator=g, device="cuda", dtype=torch.bfloat16) for _ in range(4))
+    assert q.numel() > (1 << 31)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    o, lse = fa.forward(q, k, v, scale=scale, causal=True)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=scale, causal=True)
+    fa.fa_check_device_status()
+    w = Workload("past_2_31", 1, 1, N, d, "bf16", True)
+    for i in (0, h_star - 1, h_star, h_star + 1, B * H - 1):
+        b, h = divmod(i, H)
+        one = lambda t: t[b, h][None, None].cpu()
+        q1, k1, v1, do1 = (one(t) for t in (q, k, v, do))
+        O_ref, L_ref = oracle.attention_forward(q1, k1, v1, scale, True)
+        parity.compare_o(w, parity.to_np(one(o)), O_ref, f"O head {i}")
+        parity.compare_l(one(lse).numpy().astype(np.float64), L_ref)
+        rdq, rdk, rdv, _ = oracle.attention_backward(q1, k1, v1, do1, scale, True)
+        parity.compare_g(parity.to_np(one(dq)), rdq, f"dQ head {i}")
+        parity.compare_g(parity.to_np(one(dk)), rdk, f"dK head {i}")
+        parity.compare_g(parity.to_np(one(dv)), rdv, f"dV head {i}")
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+
+
 def test_forward_allocates_nothing_beyond_its_outputs():
     """O(N) memory: at N = 32768 a single fp32 score matrix of one head would take
     4.3 GB; the forward call's footprint is its two outputs (allocated by torch in
