@@ -37,6 +37,12 @@
  * `stream`; a kernel that gave up on a bounded device-side wait records it in a
  * device error word, which `fa_check_device_status` reports (it synchronizes
  * the stream).  No kernel traps.
+ *
+ * Threads: calls may come from several host threads on different streams; the
+ * device-buffer entry points share no host state between calls but the device
+ * error record (one per device: a status check reports, and clears, what any
+ * call on that device recorded) and the measurement hook (one per process, not
+ * thread-safe).  The host-buffer entry points serialize themselves.
  */
 #ifndef FA_ATTENTION_H_
 #define FA_ATTENTION_H_
