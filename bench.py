@@ -505,6 +505,8 @@ def main():
         clocks.__exit__(None, None, None)
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
     e2e_value = world * flops_step * K / (e2e_ms / 1e3) / 1e12
+    # spread of the single steps (rank 0): the host copies' speed varies from run to run
+    e2e_steps = sorted(a.elapsed_time(b) for a, b in e2e_ev)
 
     # ---- roofline: every main kernel on its own, the dominant one as the `roofline` entry.
     # Algorithmic FLOPs (forward 4d per visible pair, backward 10d: the five products S, dP,
@@ -590,6 +592,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / K,
+                    "step_ms_min_median_max": [e2e_steps[0], statistics.median(e2e_steps), e2e_steps[-1]],
                     "path": f"{'fa_fwd_host' if fwd_only else 'fa_fwd_bwd_host'} (C ABI, pinned host buffers, "
                             f"{args.chunks if args.chunks > 0 else 'default'} head chunks)"},
             "gpu_launches": (1 if fwd_only else n_launch + 1) * K,  # + the D pre-pass
