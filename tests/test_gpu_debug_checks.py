@@ -89,6 +89,32 @@ def test_checked_build_runs_parity_cases_clean(dlib, w):
     parity.compare_g(parity.to_np(dv), rdv, "dV")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_checked_build_past_two_to_the_31_elements(dlib, d):
+    """The checked build on tensors of more than 2^31 elements (the heads past
+    h* = 2^31 / (N d) sit beyond any 32-bit element offset): every tensor-map
+    coordinate, tensor-memory column and barrier phase check stays silent."""
+    N = 1024
+    B, H = 2, (1 << 31) // (N * d) // 2 + 8
+    torch.cuda.empty_cache()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(20000 + d)
+    q, k, v, do = (torch.randn(B, H, N, d, generator=g, device="cuda", dtype=torch.bfloat16) for _ in range(4))
+    assert q.numel() > (1 << 31)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(dlib.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    sc = ctypes.c_float(float(np.float32(1.0 / np.sqrt(d))))
+    assert status(dlib)[0] == FA_OK
+    assert dlib.fa_fwd_ex(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, H, N, N, d, sc, 1, 1, _stream()) == FA_OK
+    assert dlib.fa_bwd_ex(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv), _p(ws), ws.numel(),
+                          B, H, H, N, N, d, sc, 1, 1, _stream()) == FA_OK
+    code, rec = status(dlib)
+    assert code == FA_OK, f"a device-side check fired: record {rec}"
+    del q, k, v, do, o, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("kind", range(1, 8))
 def test_each_check_reports_a_planted_violation(dlib, kind):
     assert status(dlib)[0] == FA_OK
